@@ -1,0 +1,270 @@
+"""Python binding of the GB300 multi-LoRA segmented linear (C ABI in include/lora.h).
+
+Argument marshalling only: every step of the path runs in the CUDA library
+``_lib/liblora_gb300.so``.  PyTorch supplies device memory and streams.  There is no
+CPU or PyTorch fallback: if the library is missing or fails to load, importing this
+package raises.
+
+Same names as the C ABI (``lora_pool_bytes``, ``lora_pool_create``,
+``lora_pool_load_slot``, ``lora_pool_unload_slot``, ``lora_segment``,
+``lora_segment_status``, ``lora_linear_workspace_bytes``, ``lora_linear_fwd``,
+``lora_linear_policy``, ``lora_last_error``), plus a small ``LoraPool`` convenience
+wrapper that owns the pool's device buffer.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "liblora_gb300.so")
+
+LORA_F32, LORA_F16, LORA_BF16 = 0, 1, 2
+LORA_OK, LORA_EINVAL, LORA_ESLOT, LORA_EBUSY, LORA_ERANK = 0, -1, -2, -3, -4
+LORA_ENOSPACE, LORA_EIDX, LORA_ECUDA, LORA_EUNSUP, LORA_ETIMEOUT = -5, -6, -7, -8, -9
+LORA_VARIANT_AUTO, LORA_VARIANT_FUSED, LORA_VARIANT_SEPARATE, LORA_VARIANT_CUDA_CORE = 0, 1, 2, 3
+
+TORCH_TO_LORA = {torch.float32: LORA_F32, torch.float16: LORA_F16, torch.bfloat16: LORA_BF16}
+
+EXPORTED = (
+    "lora_pool_bytes", "lora_pool_create", "lora_pool_destroy", "lora_pool_load_slot", "lora_pool_unload_slot",
+    "lora_segment_workspace_bytes", "lora_segment", "lora_segment_status", "lora_linear_workspace_bytes",
+    "lora_linear_fwd", "lora_linear_policy", "lora_last_error", "lora_kernel_launch_count",
+)
+
+
+class LoraError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class lora_pool_desc(ctypes.Structure):
+    _fields_ = [("h_in", ctypes.c_int32), ("h_out", ctypes.c_int32), ("r_max", ctypes.c_int32),
+                ("n_slots", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class lora_segments(ctypes.Structure):
+    _fields_ = [("perm_dev", ctypes.c_void_p), ("seg_start_dev", ctypes.c_void_p), ("seg_slot_dev", ctypes.c_void_p),
+                ("nseg_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p), ("idx_dev", ctypes.c_void_p),
+                ("n_tokens", ctypes.c_int32), ("n_slots", ctypes.c_int32)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+                          " (there is no fallback path)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    P = ctypes.POINTER
+    sig = {
+        "lora_pool_bytes": [P(lora_pool_desc), P(sz)],
+        "lora_pool_create": [P(lora_pool_desc), vp, sz, vp, P(vp)],
+        "lora_pool_destroy": [vp],
+        "lora_pool_load_slot": [vp, i32, vp, vp, i32, ctypes.c_float, vp],
+        "lora_pool_unload_slot": [vp, i32, vp],
+        "lora_segment_workspace_bytes": [i32, i32, P(sz)],
+        "lora_segment": [vp, i32, vp, vp, sz, P(lora_segments), vp],
+        "lora_segment_status": [P(lora_segments), vp, P(i32)],
+        "lora_linear_workspace_bytes": [vp, i32, P(sz)],
+        "lora_linear_fwd": [vp, vp, vp, vp, P(lora_segments), i32, vp, sz, vp],
+        "lora_linear_policy": [vp, i32, P(i32)],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.lora_last_error.argtypes = []
+    lib.lora_last_error.restype = ctypes.c_char_p
+    lib.lora_kernel_launch_count.argtypes = []
+    lib.lora_kernel_launch_count.restype = ctypes.c_uint64
+    return lib
+
+
+_lib = _load()
+
+
+def lora_last_error() -> str:
+    return _lib.lora_last_error().decode()
+
+
+def lora_kernel_launch_count() -> int:
+    return int(_lib.lora_kernel_launch_count())
+
+
+def _check(rc: int) -> None:
+    if rc != LORA_OK:
+        raise LoraError(rc, lora_last_error())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ---- same-named wrappers of the C ABI ------------------------------------------------------
+
+def lora_pool_bytes(h_in: int, h_out: int, r_max: int, n_slots: int, dtype: torch.dtype) -> int:
+    d = lora_pool_desc(h_in, h_out, r_max, n_slots, TORCH_TO_LORA[dtype])
+    out = ctypes.c_size_t()
+    _check(_lib.lora_pool_bytes(ctypes.byref(d), ctypes.byref(out)))
+    return out.value
+
+
+def lora_pool_create(h_in: int, h_out: int, r_max: int, n_slots: int, dtype: torch.dtype, dev_mem: torch.Tensor,
+                     stream=None) -> ctypes.c_void_p:
+    d = lora_pool_desc(h_in, h_out, r_max, n_slots, TORCH_TO_LORA[dtype])
+    h = ctypes.c_void_p()
+    _check(_lib.lora_pool_create(ctypes.byref(d), _ptr(_dev(dev_mem, "dev_mem")),
+                                 dev_mem.numel() * dev_mem.element_size(), _stream(stream), ctypes.byref(h)))
+    return h
+
+
+def lora_pool_destroy(handle) -> None:
+    _check(_lib.lora_pool_destroy(handle))
+
+
+def lora_pool_load_slot(handle, slot: int, A: torch.Tensor, B: torch.Tensor, rank: int, alpha: float,
+                        stream=None) -> None:
+    _check(_lib.lora_pool_load_slot(handle, slot, _ptr(_dev(A, "A")), _ptr(_dev(B, "B")), rank, float(alpha),
+                                    _stream(stream)))
+
+
+def lora_pool_unload_slot(handle, slot: int, stream=None) -> None:
+    _check(_lib.lora_pool_unload_slot(handle, slot, _stream(stream)))
+
+
+def lora_segment_workspace_bytes(n_tokens: int, n_slots: int) -> int:
+    out = ctypes.c_size_t()
+    _check(_lib.lora_segment_workspace_bytes(n_tokens, n_slots, ctypes.byref(out)))
+    return out.value
+
+
+def lora_segment(idx: torch.Tensor, pool_handle, ws: torch.Tensor, stream=None) -> lora_segments:
+    if idx.dtype != torch.int32:
+        raise ValueError("idx must be int32")
+    seg = lora_segments()
+    _check(_lib.lora_segment(_ptr(_dev(idx, "idx")) if idx.numel() else ctypes.c_void_p(0), idx.numel(), pool_handle,
+                             _ptr(_dev(ws, "ws")), ws.numel() * ws.element_size(), ctypes.byref(seg),
+                             _stream(stream)))
+    return seg
+
+
+def lora_segment_status(seg: lora_segments, stream=None) -> int:
+    out = ctypes.c_int()
+    _check(_lib.lora_segment_status(ctypes.byref(seg), _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def lora_linear_workspace_bytes(pool_handle, n_tokens: int) -> int:
+    out = ctypes.c_size_t()
+    _check(_lib.lora_linear_workspace_bytes(pool_handle, n_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def lora_linear_policy(pool_handle, n_tokens: int) -> int:
+    out = ctypes.c_int()
+    _check(_lib.lora_linear_policy(pool_handle, n_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def lora_linear_fwd(pool_handle, W: torch.Tensor, x: torch.Tensor, y: torch.Tensor, seg: lora_segments,
+                    ws: torch.Tensor, variant: int = LORA_VARIANT_AUTO, stream=None) -> torch.Tensor:
+    _check(_lib.lora_linear_fwd(pool_handle, _ptr(_dev(W, "W")), _ptr(_dev(x, "x")), _ptr(_dev(y, "y")),
+                                ctypes.byref(seg), variant, _ptr(_dev(ws, "ws")), ws.numel() * ws.element_size(),
+                                _stream(stream)))
+    return y
+
+
+def segment_arrays(seg: lora_segments) -> dict:
+    """Views (int32 device tensors) of the segment outputs inside the workspace ``seg._ws``."""
+    ws = seg._ws
+    base = ws.data_ptr()
+    n, S = int(seg.n_tokens), int(seg.n_slots)
+
+    def view(ptr, count):
+        off = int(ptr) - base
+        return ws[off:off + 4 * count].view(torch.int32)
+
+    return {"perm": view(seg.perm_dev, n), "seg_start": view(seg.seg_start_dev, S + 2),
+            "seg_slot": view(seg.seg_slot_dev, S + 1), "nseg": view(seg.nseg_dev, 1),
+            "status": view(seg.status_dev, 1), "idx": view(seg.idx_dev, n)}
+
+
+# ---- convenience ----------------------------------------------------------------------------
+
+def _device_bytes(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte aligned, zero-filled device byte buffer (torch's allocator aligns to 512)."""
+    t = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+    assert t.data_ptr() % 256 == 0
+    return t
+
+
+class LoraPool:
+    """One adapter pool (one linear layer) in a device buffer this object owns."""
+
+    def __init__(self, h_in: int, h_out: int, r_max: int, n_slots: int, dtype: torch.dtype, device="cuda",
+                 stream=None):
+        self.h_in, self.h_out, self.r_max, self.n_slots, self.dtype = h_in, h_out, r_max, n_slots, dtype
+        self.nbytes = lora_pool_bytes(h_in, h_out, r_max, n_slots, dtype)
+        self.mem = _device_bytes(self.nbytes, device)
+        self.handle = lora_pool_create(h_in, h_out, r_max, n_slots, dtype, self.mem, stream)
+        self._ws = {}
+
+    def load_slot(self, slot: int, A: torch.Tensor, B: torch.Tensor, alpha: float, stream=None) -> None:
+        lora_pool_load_slot(self.handle, slot, A, B, int(A.shape[0]), alpha, stream)
+
+    def unload_slot(self, slot: int, stream=None) -> None:
+        lora_pool_unload_slot(self.handle, slot, stream)
+
+    def segment_workspace(self, n_tokens: int, device="cuda") -> torch.Tensor:
+        return _device_bytes(lora_segment_workspace_bytes(n_tokens, self.n_slots), device)
+
+    def linear_workspace(self, n_tokens: int, device="cuda") -> torch.Tensor:
+        return _device_bytes(lora_linear_workspace_bytes(self.handle, n_tokens), device)
+
+    def segment(self, idx: torch.Tensor, ws: Optional[torch.Tensor] = None, stream=None):
+        if ws is None:
+            ws = self.segment_workspace(idx.numel(), idx.device)
+        seg = lora_segment(idx, self.handle, ws, stream)
+        seg._ws = ws  # keep the workspace alive with the segments
+        return seg
+
+    def linear(self, W: torch.Tensor, x: torch.Tensor, seg, variant: int = LORA_VARIANT_AUTO,
+               y: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        n = int(seg.n_tokens)
+        if y is None:
+            y = torch.empty((n, self.h_out), dtype=self.dtype, device=x.device)
+        if ws is None:
+            key = (n, x.device)
+            if key not in self._ws:
+                self._ws[key] = self.linear_workspace(n, x.device)
+            ws = self._ws[key]
+        return lora_linear_fwd(self.handle, W, x, y, seg, ws, variant, stream)
+
+    def close(self) -> None:
+        if self.handle is not None:
+            lora_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

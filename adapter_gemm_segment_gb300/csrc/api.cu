@@ -1,0 +1,157 @@
+// C ABI of the LoRA-augmented linear: workspace sizing, argument checks, variant policy and
+// the launch sequence shrink -> base GEMM (+ fused expand) [-> separate expand].
+//
+// Variant policy: the blog.lonae.com page ("LLM 多 LoRA 推理服务工程 2026") reports that on
+// A100/H100 the fused kernel wins from batch 8 up and the separate kernel at batch 1, and
+// asks for the fused/separate threshold to be tuned per GPU model.  The threshold below is the
+// one measured on GB300 (see the policy sweep of the benchmark).
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+static thread_local char g_err[512] = "";
+static std::atomic<uint64_t> g_launches{0};
+
+int set_error(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
+
+int num_sms() {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+    }
+    return sms;
+}
+
+// Fused expand from this many tokens up; below it the separate residual kernel.
+constexpr int kFusedMinTokens = 1;
+constexpr int kVariantCudaCore = LORA_VARIANT_CUDA_CORE;
+
+struct LinWsLayout {
+    size_t s_off, cnt_off, part_off, total;
+    int counters;
+    size_t partial_floats;
+};
+
+static LinWsLayout lin_layout(const PoolView& pv, int n) {
+    LinWsLayout L;
+    size_t o = 0;
+    L.s_off = o;
+    o += align256(sizeof(float) * (size_t)(n > 0 ? n : 1) * pv.R);
+    int counters = 0;
+    const size_t pf = tc_workspace_floats(pv, n, &counters);
+    L.counters = counters;
+    L.partial_floats = pf;
+    L.cnt_off = o;
+    o += align256(sizeof(int32_t) * (size_t)(counters > 0 ? counters : 1));
+    L.part_off = o;
+    o += align256(sizeof(float) * (pf > 0 ? pf : 1));
+    L.total = o;
+    return L;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+const char* lora_last_error(void) { return g_err; }
+
+uint64_t lora_kernel_launch_count(void) { return g_launches.load(); }
+
+int lora_linear_workspace_bytes(lora_pool_t pool, int n_tokens, size_t* bytes) {
+    if (!pool || !bytes) return set_error(LORA_EINVAL, "pool/bytes is NULL");
+    if (n_tokens < 0) return set_error(LORA_EINVAL, "n_tokens < 0");
+    *bytes = lin_layout(pool_view(pool), n_tokens).total;
+    return LORA_OK;
+}
+
+int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant) {
+    if (!pool || !variant) return set_error(LORA_EINVAL, "pool/variant is NULL");
+    *variant = n_tokens >= kFusedMinTokens ? LORA_VARIANT_FUSED : LORA_VARIANT_SEPARATE;
+    return LORA_OK;
+}
+
+int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev, const lora_segments* seg,
+                    int variant, void* ws_dev, size_t ws_bytes, void* stream) {
+    if (!pool || !seg) return set_error(LORA_EINVAL, "pool/seg is NULL");
+    const PoolView pv = pool_view(pool);
+    const int n = seg->n_tokens;
+    if (seg->n_slots != pv.S)
+        return set_error(LORA_EINVAL, "segments were built for %d slots, pool has %d", seg->n_slots, pv.S);
+    if (variant < LORA_VARIANT_AUTO || variant > kVariantCudaCore) return set_error(LORA_EINVAL, "bad variant %d", variant);
+    if (n == 0) return LORA_OK;
+    if (!W_dev || !x_dev || !y_dev || !ws_dev) return set_error(LORA_EINVAL, "W/x/y/ws is NULL");
+    if (reinterpret_cast<uintptr_t>(ws_dev) % 256) return set_error(LORA_EINVAL, "ws must be 256-byte aligned");
+    if (pv.dtype != LORA_F32) {
+        if ((reinterpret_cast<uintptr_t>(W_dev) | reinterpret_cast<uintptr_t>(x_dev) |
+             reinterpret_cast<uintptr_t>(y_dev)) % 16)
+            return set_error(LORA_EINVAL, "W/x/y must be 16-byte aligned");
+    } else if ((reinterpret_cast<uintptr_t>(W_dev) | reinterpret_cast<uintptr_t>(x_dev) |
+                reinterpret_cast<uintptr_t>(y_dev)) % 4) {
+        return set_error(LORA_EINVAL, "W/x/y must be 4-byte aligned");
+    }
+    const LinWsLayout L = lin_layout(pv, n);
+    if (ws_bytes < L.total) return set_error(LORA_ENOSPACE, "linear workspace needs %zu bytes, got %zu", L.total, ws_bytes);
+    char* w = static_cast<char*>(ws_dev);
+    float* s_buf = reinterpret_cast<float*>(w + L.s_off);
+    if (variant == LORA_VARIANT_AUTO) lora_linear_policy(pool, n, &variant);
+    const SegView sv = seg_view(seg);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const bool tc = variant != kVariantCudaCore && tc_supported(pv, n);
+    const bool fused = variant != LORA_VARIANT_SEPARATE;
+    int rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256);
+    if (rc) return rc;
+    if (tc) {
+        TcWorkspace tw;
+        tw.partials = reinterpret_cast<float*>(w + L.part_off);
+        tw.counters = reinterpret_cast<int32_t*>(w + L.cnt_off);
+        tw.partial_floats = L.partial_floats;
+        tw.counter_count = L.counters;
+        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, tw, st);
+    } else {
+        rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, st);
+    }
+    if (rc) return rc;
+    if (!fused) {
+        rc = launch_expand(pv, sv, s_buf, y_dev, st);
+        if (rc) return rc;
+    }
+    return LORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// Internal definitions shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/lora.h"
+
+// Host handle of one pool (opaque to callers of the C ABI).
+struct lora_pool {
+    lora_pool_desc desc;
+    char* base;
+    size_t bytes;
+    void* table;  // lora::SlotEntry[n_slots]
+    void* A;
+    void* B;
+    std::vector<uint8_t> mounted;  // host mirror of the slot states this handle enqueued
+};
+
+namespace lora {
+
+// Slot table entry as stored in device memory (16 bytes).
+struct SlotEntry {
+    int32_t rank;   // true rank of the mounted adapter (0 when empty)
+    int32_t state;  // kSlotEmpty / kSlotReady
+    float scale;    // alpha / rank
+    int32_t reserved;
+};
+static_assert(sizeof(SlotEntry) == 16, "slot entry layout");
+
+constexpr int32_t kSlotEmpty = 0;
+constexpr int32_t kSlotReady = 1;
+constexpr int kMaxSlots = 2048;
+constexpr int kMaxRank = 256;
+
+// Everything a compute kernel needs to know about one pool.
+struct PoolView {
+    const SlotEntry* table;
+    const void* A;  // [S, R, h_in]
+    const void* B;  // [S, h_out, R]
+    int h_in, h_out, R, S;
+    int dtype;      // lora_dtype
+};
+
+// Segments as the kernels see them (device pointers).
+struct SegView {
+    const int32_t* perm;
+    const int32_t* seg_start;
+    const int32_t* seg_slot;
+    const int32_t* nseg;
+    int32_t* status;
+    const int32_t* idx;
+    int n;
+};
+
+inline SegView seg_view(const lora_segments* s) {
+    SegView v;
+    v.perm = s->perm_dev;
+    v.seg_start = s->seg_start_dev;
+    v.seg_slot = s->seg_slot_dev;
+    v.nseg = s->nseg_dev;
+    v.status = s->status_dev;
+    v.idx = s->idx_dev;
+    v.n = s->n_tokens;
+    return v;
+}
+
+inline size_t dtype_size(int dt) { return dt == LORA_F32 ? 4 : 2; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+PoolView pool_view(const lora_pool_t p);
+
+// Host-side error reporting (thread-local message), defined in api.cu.
+int set_error(int code, const char* fmt, ...);
+void count_launch(int n = 1);
+
+// Launch helper attributes: every kernel of the hot path is launched with programmatic
+// stream serialisation so that its prologue overlaps the tail of the previous kernel;
+// each kernel waits (griddepcontrol.wait) before touching data an earlier kernel wrote.
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args);
+
+// ---- device helpers -----------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Unpack 8 16-bit values held in a uint4 to floats.
+template <typename T> __device__ __forceinline__ void unpack8(const uint4& v, float* f);
+template <> __device__ __forceinline__ void unpack8<__half>(const uint4& v, float* f) {
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 p = __half22float2(h[i]);
+        f[2 * i] = p.x;
+        f[2 * i + 1] = p.y;
+    }
+}
+template <> __device__ __forceinline__ void unpack8<__nv_bfloat16>(const uint4& v, float* f) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+}  // namespace lora
+
+#define LORA_CUDA_TRY(expr)                                                                 \
+    do {                                                                                    \
+        cudaError_t _e = (expr);                                                            \
+        if (_e != cudaSuccess)                                                              \
+            return ::lora::set_error(LORA_ECUDA, "%s: %s", #expr, cudaGetErrorString(_e));  \
+    } while (0)

@@ -1,0 +1,617 @@
+// Tensor-core base GEMM of the LoRA-augmented linear on sm_103a (tcgen05 + TMEM + TMA),
+// with the LoRA expand fused into the epilogue.
+//
+// The "fused kernel" design of the adapter execution unit ("LLM 多 LoRA 推理服务工程 2026：
+// 从热插拔到租户编排", blog.lonae.com) computes the base linear and the A/B product in one
+// launch; here the base product x W^T accumulates in tensor memory and the epilogue adds
+// scale_s * s[t,:] B_s^T (s from the shrink kernel, scale folded in) before rounding y once.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues tcgen05.mma
+// from one thread, warps 2..5 drain the accumulator (warp w may only touch TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31).  A ring of shared-memory stages with full/empty mbarriers
+// connects producer and MMA; tcgen05.commit releases stages and publishes accumulators.
+//
+// Decode (n <= 256 tokens): swap-AB.  The weight tile (128 output features) is the MMA M side
+// and the tokens (padded to a multiple of 16) the N side, so the whole batch is one N tile and
+// W streams through exactly once.  K is split over CTAs to fill the GPU; partial sums go to a
+// float32 workspace and the last CTA of each tile (arrival counter) reduces them in split
+// order, adds the LoRA term and stores y.
+//
+// Prefill (n > 256): 128-token x 256-feature tiles, persistent CTAs over the tile list,
+// double-buffered accumulators (2 x 256 TMEM columns) so the epilogue of one tile overlaps the
+// main loop of the next.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace lora {
+namespace tc {
+
+using namespace ptx;
+
+constexpr int BM = 128;       // MMA M
+constexpr int BK = 64;        // K per stage (one 128-byte swizzle row of 16-bit elements)
+constexpr int UMMA_K = 16;    // K per tcgen05.mma of kind::f16
+constexpr int kThreads = 192;
+constexpr int kPrefillBN = 256;
+constexpr int kDecodeMaxN = 256;
+constexpr int kSmemBudget = 200 * 1024;
+
+struct DecodeArgs {
+    PoolView pool;
+    SegView seg;
+    const float* s_in;
+    void* y;
+    float* partials;
+    int32_t* counters;
+    int n, n_pad, kb_total, splits, kb_per_split, stages, tmem_cols, fuse, bf16;
+};
+
+struct PrefillArgs {
+    PoolView pool;
+    SegView seg;
+    const float* s_in;
+    void* y;
+    int n, m_tiles, n_tiles, kb_total, stages, fuse, bf16;
+};
+
+// LoRA term of one (token, feature): sum_j s[t, j] * B_slot[o, j]; s already carries alpha/r.
+template <typename T>
+__device__ __forceinline__ float lora_term(const T* __restrict__ Brow, const float* __restrict__ srow, int R) {
+    float acc = 0.f;
+    for (int j = 0; j < R; j += 8) {
+        float b[8];
+        unpack8<T>(__ldg(reinterpret_cast<const uint4*>(Brow + j)), b);
+        const float4 s0 = __ldcg(reinterpret_cast<const float4*>(srow + j));
+        const float4 s1 = __ldcg(reinterpret_cast<const float4*>(srow + j + 4));
+        acc = fmaf(b[0], s0.x, acc);
+        acc = fmaf(b[1], s0.y, acc);
+        acc = fmaf(b[2], s0.z, acc);
+        acc = fmaf(b[3], s0.w, acc);
+        acc = fmaf(b[4], s1.x, acc);
+        acc = fmaf(b[5], s1.y, acc);
+        acc = fmaf(b[6], s1.z, acc);
+        acc = fmaf(b[7], s1.w, acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ void report_timeout(int32_t* status) { atomicExch(status, LORA_ETIMEOUT); }
+
+// ============================================================================================
+// decode: swap-AB + split-K
+// ============================================================================================
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stages = a.stages;
+    const uint32_t w_bytes = BM * BK * 2;
+    const uint32_t x_bytes = static_cast<uint32_t>(a.n_pad) * BK * 2;
+    const uint32_t stage_bytes = w_bytes + x_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
+    uint64_t* empty = full + stages;
+    uint64_t* tmem_full = empty + stages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort, last CTA, go
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x, split = blockIdx.y;
+    const int kb0 = split * a.kb_per_split;
+    const int nkb = min(a.kb_total, kb0 + a.kb_per_split) - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tmem_full, 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // W does not depend on earlier kernels: fill the whole ring with W tiles first, then
+            // wait for the previous grid before reading x.
+            const int pre = min(stages, nkb);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], stage_bytes);
+                tma_load_2d(smem + i * stage_bytes, &tmW, &full[i], (kb0 + i) * BK, m_tile * BM);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(smem + i * stage_bytes + w_bytes, &tmX, &full[i], (kb0 + i) * BK, 0);
+            int issued = pre;
+            for (int i = pre; i < nkb; ++i) {
+                const int s = i % stages;
+                const uint32_t ph = (i / stages) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1, flags)) break;
+                mbar_arrive_expect_tx(&full[s], stage_bytes);
+                tma_load_2d(smem + s * stage_bytes, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM);
+                tma_load_2d(smem + s * stage_bytes + w_bytes, &tmX, &full[s], (kb0 + i) * BK, 0);
+                ++issued;
+            }
+            if (flags[0]) {  // aborted: let copies already in flight land before the CTA exits
+                report_timeout(a.seg.status);
+                for (int i = max(0, issued - stages); i < issued; ++i) {
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BM, a.n_pad, a.bf16 != 0);
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % stages;
+                if (!mbar_wait(&full[s], (i / stages) & 1, flags)) {
+                    report_timeout(a.seg.status);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t wa = smem_u32(smem + s * stage_bytes);
+                const uint32_t xa = wa + w_bytes;
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k)
+                    umma_f16(tmem, sdesc_sw128(wa + k * UMMA_K * 2), sdesc_sw128(xa + k * UMMA_K * 2), idesc,
+                             (i > 0 || k > 0) ? 1u : 0u);
+                umma_commit(&empty[s]);
+            }
+            umma_commit(tmem_full);  // also on abort: fires once the issued MMAs have finished
+        }
+    } else {
+        // ---- epilogue: warps 2..5, thread <-> output feature (TMEM lane) ----
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int o = m_tile * BM + row;
+        const int h_out = a.pool.h_out, R = a.pool.R, n = a.n;
+        const bool got = mbar_wait(tmem_full, 0, flags);
+        tc_fence_after();
+        pdl_wait();
+        const int status = __ldcg(a.seg.status);
+        // one decision for all four epilogue warps (they meet at named barriers below)
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 64) flags[2] = (got && !flags[0] && status == LORA_OK) ? 1 : 0;
+        named_bar_sync(1, 128);
+        if (flags[2]) {
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            const T* B = static_cast<const T*>(a.pool.B);
+            T* y = static_cast<T*>(a.y);
+            if (a.splits == 1) {
+                for (int c0 = 0; c0 < a.n_pad; c0 += 16) {
+                    uint32_t r[16];
+                    __syncwarp();
+                    tmem_ld16(taddr + c0, r);
+                    tmem_ld_wait();
+                    if (o < h_out) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int t = c0 + c;
+                            if (t < n) {
+                                float v = __uint_as_float(r[c]);
+                                if (a.fuse) {
+                                    const int s = __ldcg(a.seg.idx + t);
+                                    if (s >= 0)
+                                        v += lora_term<T>(B + ((size_t)s * h_out + o) * R, a.s_in + (size_t)t * R, R);
+                                }
+                                y[(size_t)t * h_out + o] = from_f32<T>(v);
+                            }
+                        }
+                    }
+                }
+            } else {
+                float* part = a.partials + (size_t)(m_tile * a.splits + split) * a.n_pad * BM;
+                for (int c0 = 0; c0 < a.n_pad; c0 += 16) {
+                    uint32_t r[16];
+                    __syncwarp();
+                    tmem_ld16(taddr + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) __stcg(part + (size_t)(c0 + c) * BM + row, __uint_as_float(r[c]));
+                }
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (threadIdx.x == 64) {
+                    const int prev = atomicAdd(a.counters + m_tile, 1);
+                    flags[1] = (prev == a.splits - 1) ? 1 : 0;
+                }
+                named_bar_sync(1, 128);
+                if (flags[1]) {
+                    __threadfence();
+                    const float* tile_part = a.partials + (size_t)m_tile * a.splits * a.n_pad * BM;
+                    if (o < h_out) {
+                        for (int t = 0; t < n; ++t) {
+                            float v = 0.f;
+                            for (int sp = 0; sp < a.splits; ++sp)
+                                v += __ldcg(tile_part + ((size_t)sp * a.n_pad + t) * BM + row);
+                            if (a.fuse) {
+                                const int s = __ldcg(a.seg.idx + t);
+                                if (s >= 0)
+                                    v += lora_term<T>(B + ((size_t)s * h_out + o) * R, a.s_in + (size_t)t * R, R);
+                            }
+                            y[(size_t)t * h_out + o] = from_f32<T>(v);
+                        }
+                    }
+                    if (threadIdx.x == 64) a.counters[m_tile] = 0;  // leave the counter at rest
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ============================================================================================
+// prefill: persistent 128 x 256 tiles, double-buffered accumulators
+// ============================================================================================
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    const PrefillArgs a) {
+    constexpr int BN = kPrefillBN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stages = a.stages;
+    constexpr uint32_t x_bytes = BM * BK * 2;
+    constexpr uint32_t w_bytes = BN * BK * 2;
+    constexpr uint32_t stage_bytes = x_bytes + w_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
+    uint64_t* empty = full + stages;
+    uint64_t* acc_full = empty + stages;  // [2]
+    uint64_t* acc_empty = acc_full + 2;   // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = a.m_tiles * a.n_tiles;
+    const int nkb = a.kb_total;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+        }
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 2 * BN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;
+            bool waited = false;
+            int deferred = 0;
+            int def_kb[16], def_m[16];
+            for (int tile = blockIdx.x; tile < total && !flags[0]; tile += gridDim.x) {
+                const int m0 = (tile / a.n_tiles) * BM;
+                const int n0 = (tile % a.n_tiles) * BN;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % stages;
+                    const uint32_t ph = (it / stages) & 1;
+                    if (it >= stages && !mbar_wait(&empty[s], ph ^ 1, flags)) break;
+                    mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    tma_load_2d(smem + s * stage_bytes + x_bytes, &tmW, &full[s], kb * BK, n0);
+                    if (waited) {
+                        tma_load_2d(smem + s * stage_bytes, &tmX, &full[s], kb * BK, m0);
+                    } else {
+                        // first ring pass: weights first, x after the previous grid finished
+                        def_kb[deferred] = kb;
+                        def_m[deferred] = m0;
+                        ++deferred;
+                        if (deferred == stages) {
+                            pdl_wait();
+                            waited = true;
+                            for (int d = 0; d < deferred; ++d)
+                                tma_load_2d(smem + d * stage_bytes, &tmX, &full[d], def_kb[d] * BK, def_m[d]);
+                        }
+                    }
+                }
+            }
+            if (!waited) {
+                pdl_wait();
+                for (int d = 0; d < deferred; ++d)
+                    tma_load_2d(smem + d * stage_bytes, &tmX, &full[d], def_kb[d] * BK, def_m[d]);
+            }
+            if (flags[0]) {
+                report_timeout(a.seg.status);
+                for (int i = max(0, it - stages); i < it; ++i) {
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BM, BN, a.bf16 != 0);
+            int it = 0, local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+                const int buf = local & 1;
+                const uint32_t acc = tmem + buf * BN;
+                if (!mbar_wait(&acc_empty[buf], ((local >> 1) & 1) ^ 1, flags)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % stages;
+                    if (!mbar_wait(&full[s], (it / stages) & 1, flags)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xa = smem_u32(smem + s * stage_bytes);
+                    const uint32_t wa = xa + x_bytes;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        umma_f16(acc, sdesc_sw128(xa + k * UMMA_K * 2), sdesc_sw128(wa + k * UMMA_K * 2), idesc,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(&empty[s]);
+                }
+                umma_commit(&acc_full[buf]);
+            }
+            if (!ok) report_timeout(a.seg.status);
+        }
+    } else {
+        // ---- epilogue: thread <-> token row (TMEM lane), 256 features per tile ----
+        const int q = warp & 3;
+        const int h_out = a.pool.h_out, R = a.pool.R, n = a.n;
+        const T* B = static_cast<const T*>(a.pool.B);
+        T* y = static_cast<T*>(a.y);
+        bool waited = false;
+        int status = LORA_OK;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+            const int buf = local & 1;
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (local >> 1) & 1, flags));
+            if (!got) break;
+            tc_fence_after();
+            if (!waited) {
+                pdl_wait();
+                status = __ldcg(a.seg.status);
+                waited = true;
+            }
+            const int m0 = (tile / a.n_tiles) * BM;
+            const int n0 = (tile % a.n_tiles) * BN;
+            const int t = m0 + q * 32 + lane;
+            const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
+            const int slot = (a.fuse && t < n) ? __ldcg(a.seg.idx + t) : -1;
+            const float* srow = a.s_in + (size_t)(t < n ? t : 0) * R;
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                uint32_t r[16];
+                __syncwarp();
+                tmem_ld16(taddr + c0, r);
+                tmem_ld_wait();
+                if (status != LORA_OK || t >= n || n0 + c0 >= h_out) continue;  // after the warp-wide load
+                float v[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
+                if (slot >= 0) {
+                    const T* Bt = B + ((size_t)slot * h_out + n0 + c0) * R;
+                    const int cmax = min(16, h_out - (n0 + c0));
+                    for (int c = 0; c < cmax; ++c) v[c] += lora_term<T>(Bt + (size_t)c * R, srow, R);
+                }
+                T* yp = y + (size_t)t * h_out + n0 + c0;
+                alignas(16) T outv[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) outv[c] = from_f32<T>(v[c]);
+                if (n0 + c0 + 16 <= h_out) {
+                    reinterpret_cast<uint4*>(yp)[0] = reinterpret_cast<const uint4*>(outv)[0];
+                    reinterpret_cast<uint4*>(yp)[1] = reinterpret_cast<const uint4*>(outv)[1];
+                } else {  // h_out is a multiple of 8: one half-chunk remains
+                    reinterpret_cast<uint4*>(yp)[0] = reinterpret_cast<const uint4*>(outv)[0];
+                }
+            }
+            tc_fence_before();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 2 * BN);
+}
+
+// ============================================================================================
+// host side
+// ============================================================================================
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Row-major [rows, cols] 16-bit matrix, box {64 columns, box_rows rows}, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+static int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return LORA_OK;
+}
+
+struct DecodePlan {
+    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols;
+    size_t smem;
+};
+
+static DecodePlan plan_decode(const PoolView& pv, int n) {
+    DecodePlan p;
+    p.n_pad = std::max(16, (n + 15) / 16 * 16);
+    p.m_tiles = (pv.h_out + BM - 1) / BM;
+    p.kb_total = (pv.h_in + BK - 1) / BK;
+    const int sms = num_sms();
+    int splits = std::max(1, sms / p.m_tiles);
+    splits = std::min(splits, std::max(1, p.kb_total / 4));
+    p.kb_per_split = (p.kb_total + splits - 1) / splits;
+    p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
+    const int stage_bytes = BM * BK * 2 + p.n_pad * BK * 2;
+    p.stages = std::max(2, std::min(8, kSmemBudget / stage_bytes));
+    p.stages = std::min(p.stages, std::max(2, p.kb_per_split));
+    int cols = 32;
+    while (cols < p.n_pad) cols <<= 1;
+    p.tmem_cols = cols;
+    p.smem = (size_t)p.stages * stage_bytes + 1024 + 256;
+    return p;
+}
+
+}  // namespace tc
+
+int tc_supported(const PoolView& pv, int n) {
+    if (pv.dtype != LORA_F16 && pv.dtype != LORA_BF16) return 0;
+    if (pv.h_in % 8 || pv.h_out % 8 || pv.R % 8) return 0;
+    (void)n;
+    return 1;
+}
+
+size_t tc_workspace_floats(const PoolView& pv, int n, int* counters) {
+    if (n <= 0 || n > tc::kDecodeMaxN || !tc_supported(pv, n)) {
+        *counters = 0;
+        return 0;
+    }
+    const tc::DecodePlan p = tc::plan_decode(pv, n);
+    *counters = p.m_tiles;
+    return p.splits > 1 ? (size_t)p.m_tiles * p.splits * p.n_pad * tc::BM : 0;
+}
+
+template <typename T>
+static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
+                       bool fuse, const TcWorkspace& ws, cudaStream_t st) {
+    using namespace tc;
+    const int n = sv.n;
+    if (n == 0) return LORA_OK;
+    const int bf16 = pv.dtype == LORA_BF16;
+    if (n <= kDecodeMaxN) {
+        const DecodePlan p = plan_decode(pv, n);
+        if (p.splits > 1 && (!ws.partials || !ws.counters || ws.partial_floats < (size_t)p.m_tiles * p.splits * p.n_pad * BM ||
+                             ws.counter_count < p.m_tiles))
+            return set_error(LORA_ENOSPACE, "decode split-K workspace too small");
+        CUtensorMap mW, mX;
+        int rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, BM);
+        if (rc) return rc;
+        rc = make_map(&mX, x, bf16, pv.h_in, n, p.n_pad);
+        if (rc) return rc;
+        DecodeArgs a;
+        a.pool = pv;
+        a.seg = sv;
+        a.s_in = s_in;
+        a.y = y;
+        a.partials = ws.partials;
+        a.counters = ws.counters;
+        a.n = n;
+        a.n_pad = p.n_pad;
+        a.kb_total = p.kb_total;
+        a.splits = p.splits;
+        a.kb_per_split = p.kb_per_split;
+        a.stages = p.stages;
+        a.tmem_cols = p.tmem_cols;
+        a.fuse = fuse ? 1 : 0;
+        a.bf16 = bf16;
+        static bool attr = false;
+        if (!attr) {
+            LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kSmemBudget + 8 * 1024));
+            attr = true;
+        }
+        void* args[] = {(void*)&mW, (void*)&mX, (void*)&a};
+        LORA_CUDA_TRY(launch_pdl((const void*)gemm_decode_kernel<T>, dim3(p.m_tiles, p.splits), dim3(kThreads), p.smem,
+                                 st, args));
+        return LORA_OK;
+    }
+    // prefill
+    PrefillArgs a;
+    a.pool = pv;
+    a.seg = sv;
+    a.s_in = s_in;
+    a.y = y;
+    a.n = n;
+    a.m_tiles = (n + BM - 1) / BM;
+    a.n_tiles = (pv.h_out + kPrefillBN - 1) / kPrefillBN;
+    a.kb_total = (pv.h_in + BK - 1) / BK;
+    const int stage_bytes = (BM + kPrefillBN) * BK * 2;
+    a.stages = std::min(4, kSmemBudget / stage_bytes);
+    a.fuse = fuse ? 1 : 0;
+    a.bf16 = bf16;
+    CUtensorMap mX, mW;
+    int rc = make_map(&mX, x, bf16, pv.h_in, n, BM);
+    if (rc) return rc;
+    rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, kPrefillBN);
+    if (rc) return rc;
+    const size_t smem = (size_t)a.stages * stage_bytes + 1024 + 256;
+    static bool attr = false;
+    if (!attr) {
+        LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_prefill_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBudget + 8 * 1024));
+        attr = true;
+    }
+    const int total = a.m_tiles * a.n_tiles;
+    const int grid = std::min(total, num_sms());
+    void* args[] = {(void*)&mX, (void*)&mW, (void*)&a};
+    LORA_CUDA_TRY(launch_pdl((const void*)gemm_prefill_kernel<T>, dim3(grid), dim3(kThreads), smem, st, args));
+    return LORA_OK;
+}
+
+int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
+                   bool fuse, const TcWorkspace& ws, cudaStream_t st) {
+    if (pv.dtype == LORA_F16) return launch_tc_t<__half>(pv, sv, W, x, s_in, y, fuse, ws, st);
+    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, y, fuse, ws, st);
+}
+
+}  // namespace lora

@@ -1,0 +1,36 @@
+// Launchers shared between the library's translation units (host side).
+#pragma once
+#include "common.cuh"
+
+namespace lora {
+
+// s_out[t, :] = scale_s * x[t] A_s^T for every token with a slot (float32, original order).
+// tiled = one CTA per (segment, 64 tokens) through shared memory; otherwise one warp per
+// (token, 8 adapter rows).
+int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled);
+
+// y[t, :] += s[t, :] B_s^T (separate variant's residual kernel).
+int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, void* y, cudaStream_t st);
+
+// CUDA-core base GEMM y = x W^T (+ fused expand when fuse).
+int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
+                     bool fuse, cudaStream_t st);
+
+// Tensor-core (tcgen05) base GEMM with optional fused expand.
+//   decode path  (n <= 256): W tiles on the MMA M side, tokens on N, split-K with an
+//                 in-kernel last-CTA reduction (partials + counters in ws).
+//   prefill path (n > 256):  token tiles on M (128), outputs on N (256), persistent CTAs.
+struct TcWorkspace {
+    float* partials;     // decode split-K partials
+    int32_t* counters;   // decode split-K arrival counters (zero at rest)
+    size_t partial_floats;
+    int counter_count;
+};
+int tc_supported(const PoolView& pv, int n);
+size_t tc_workspace_floats(const PoolView& pv, int n, int* counters);
+int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
+                   bool fuse, const TcWorkspace& ws, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace lora

@@ -1,0 +1,364 @@
+// CUDA-core kernels of the LoRA path: the segmented shrink (x A^T), the residual expand of
+// the separate variant, and a CUDA-core base GEMM with the expand fused in its epilogue
+// (float32 pools and shapes the tensor-core path does not take).
+//
+// The execution unit of "LLM 多 LoRA 推理服务工程 2026：从热插拔到租户编排" (blog.lonae.com)
+// applies the low-rank A/B product onto the base hidden state, either inside the base
+// kernel (fused) or as a residual added by a second kernel (separate).  The shrink writes
+// s[t, j] = (alpha_s / r_s) * sum_k x[t,k] A_s[j,k] in float32 for every token t with a slot,
+// in original token order; both expands read it.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    return v;
+}
+
+// ---- shrink, one warp per (sorted token, group of RG adapter rows) ----------------------------
+// Walking tokens in sorted order keeps consecutive warps on the same adapter, so each A row
+// comes from HBM once per batch and from L1/L2 afterwards.
+template <typename T, int RG>
+__global__ void __launch_bounds__(256)
+shrink_warp_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
+    pdl_wait();
+    pdl_trigger();
+    if (*seg.status != LORA_OK) return;
+    const int lane = threadIdx.x & 31;
+    const int groups = pool.R / RG;
+    const long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const long j = gw / groups;
+    const int g = (int)(gw % groups);
+    if (j >= seg.n) return;
+    const int t = seg.perm[j];
+    const int s = seg.idx[t];
+    if (s < 0) return;
+    const float scale = pool.table[s].scale;
+    const int h = pool.h_in;
+    const T* xr = x + (size_t)t * h;
+    const T* Ar = static_cast<const T*>(pool.A) + ((size_t)s * pool.R + (size_t)g * RG) * h;
+    float acc[RG];
+#pragma unroll
+    for (int r = 0; r < RG; ++r) acc[r] = 0.f;
+    if constexpr (sizeof(T) == 2) {
+        for (int k = lane * 8; k < h; k += 256) {
+            float xf[8];
+            unpack8<T>(*reinterpret_cast<const uint4*>(xr + k), xf);
+#pragma unroll
+            for (int r = 0; r < RG; ++r) {
+                float af[8];
+                unpack8<T>(*reinterpret_cast<const uint4*>(Ar + (size_t)r * h + k), af);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[r] = fmaf(xf[e], af[e], acc[r]);
+            }
+        }
+    } else {
+        for (int k = lane; k < h; k += 32) {
+            const float xv = to_f32(xr[k]);
+#pragma unroll
+            for (int r = 0; r < RG; ++r) acc[r] = fmaf(xv, to_f32(Ar[(size_t)r * h + k]), acc[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RG; ++r) acc[r] = warp_sum(acc[r]);
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < RG; ++r) s_out[(size_t)t * pool.R + g * RG + r] = scale * acc[r];
+    }
+}
+
+// ---- shrink, tiled: one CTA per (segment, 64 sorted tokens) -----------------------------------
+// For long segments (prefill) x and A are staged through shared memory in K-chunks of 64 and
+// every thread keeps a 4 x (R/16) register tile.
+constexpr int kShrTT = 64, kShrKC = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+shrink_tiled_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
+    extern __shared__ float sh[];
+    const int R = pool.R, h = pool.h_in;
+    float* xs = sh;                             // [TT][KC+1]
+    float* as = sh + kShrTT * (kShrKC + 1);     // [R][KC+1]
+    __shared__ int s_seg, s_j0, s_j1, s_slot;
+    __shared__ int s_tok[kShrTT];
+    pdl_wait();
+    pdl_trigger();
+    if (*seg.status != LORA_OK) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (warp == 0) {
+        // locate this CTA's (segment, tile): tiles of a segment = ceil(len / TT), none for -1
+        const int nseg = *seg.nseg;
+        int run = 0;
+        int found = -1, ftile = 0;
+        for (int base = 0; base < nseg && found < 0; base += 32) {
+            const int i = base + lane;
+            int ti = 0;
+            if (i < nseg && seg.seg_slot[i] >= 0) ti = (seg.seg_start[i + 1] - seg.seg_start[i] + kShrTT - 1) / kShrTT;
+            int v = ti;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, d);
+                if (lane >= d) v += u;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, (int)blockIdx.x < run + v);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                found = base + l;
+                const int vl = __shfl_sync(0xffffffffu, v, l);
+                const int tl = __shfl_sync(0xffffffffu, ti, l);
+                ftile = (int)blockIdx.x - (run + vl - tl);
+            }
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) {
+            s_seg = found;
+            if (found >= 0) {
+                s_slot = seg.seg_slot[found];
+                s_j0 = seg.seg_start[found] + ftile * kShrTT;
+                s_j1 = min(s_j0 + kShrTT, seg.seg_start[found + 1]);
+            }
+        }
+    }
+    __syncthreads();
+    if (s_seg < 0) return;
+    const int j0 = s_j0, cnt = s_j1 - s_j0, slot = s_slot;
+    if (tid < kShrTT) s_tok[tid] = tid < cnt ? seg.perm[j0 + tid] : -1;
+    __syncthreads();
+    const T* A = static_cast<const T*>(pool.A) + (size_t)slot * R * h;
+    const int tq = tid >> 4, tr = tid & 15;
+    constexpr int MAXJ = kMaxRank / 16;
+    float acc[4][MAXJ];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < MAXJ; ++jj) acc[i][jj] = 0.f;
+    const int nj = (R + 15) / 16;
+    for (int k0 = 0; k0 < h; k0 += kShrKC) {
+        for (int e = tid; e < kShrTT * kShrKC; e += 256) {
+            const int q = e / kShrKC, kk = e % kShrKC;
+            const int t = s_tok[q];
+            xs[q * (kShrKC + 1) + kk] = (t >= 0 && k0 + kk < h) ? to_f32(x[(size_t)t * h + k0 + kk]) : 0.f;
+        }
+        for (int e = tid; e < R * kShrKC; e += 256) {
+            const int r = e / kShrKC, kk = e % kShrKC;
+            as[r * (kShrKC + 1) + kk] = (k0 + kk < h) ? to_f32(A[(size_t)r * h + k0 + kk]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < kShrKC; ++kk) {
+            float xv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xv[i] = xs[(tq + 16 * i) * (kShrKC + 1) + kk];
+#pragma unroll
+            for (int jj = 0; jj < MAXJ; ++jj) {
+                if (jj < nj && tr + 16 * jj < R) {
+                    const float av = as[(tr + 16 * jj) * (kShrKC + 1) + kk];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i][jj] = fmaf(xv[i], av, acc[i][jj]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    const float scale = pool.table[slot].scale;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = tq + 16 * i;
+        if (q >= cnt) continue;
+        const int t = s_tok[q];
+#pragma unroll
+        for (int jj = 0; jj < MAXJ; ++jj)
+            if (jj < nj && tr + 16 * jj < R) s_out[(size_t)t * R + tr + 16 * jj] = scale * acc[i][jj];
+    }
+}
+
+// ---- expand of the separate variant: y[t, o] += sum_j s[t, j] B_s[o, j] -----------------------
+// One CTA per (256 outputs, 16 tokens).  y is read, the float32 LoRA term added, and y is
+// rounded and written back (the residual add of the separate design).
+constexpr int kExpTT = 16;
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+expand_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, T* __restrict__ y) {
+    extern __shared__ float ss[];  // [TT][R]
+    __shared__ int sl[kExpTT];
+    pdl_wait();
+    pdl_trigger();
+    if (*seg.status != LORA_OK) return;
+    const int R = pool.R, h_out = pool.h_out;
+    const int t0 = blockIdx.y * kExpTT;
+    const int nt = min(kExpTT, seg.n - t0);
+    if (threadIdx.x < kExpTT) sl[threadIdx.x] = threadIdx.x < nt ? seg.idx[t0 + threadIdx.x] : -1;
+    __syncthreads();
+    for (int e = threadIdx.x; e < nt * R; e += blockDim.x) {
+        const int q = e / R;
+        ss[e] = sl[q] >= 0 ? s_in[(size_t)(t0 + q) * R + e % R] : 0.f;
+    }
+    __syncthreads();
+    const int o = blockIdx.x * 256 + threadIdx.x;
+    if (o >= h_out) return;
+    const T* B = static_cast<const T*>(pool.B);
+    for (int q = 0; q < nt; ++q) {
+        const int s = sl[q];
+        if (s < 0) continue;
+        const T* Br = B + ((size_t)s * h_out + o) * R;
+        float acc = 0.f;
+        if constexpr (sizeof(T) == 2) {
+            for (int j = 0; j < R; j += 8) {
+                float bf[8];
+                unpack8<T>(*reinterpret_cast<const uint4*>(Br + j), bf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(bf[e], ss[q * R + j + e], acc);
+            }
+        } else {
+            for (int j = 0; j < R; ++j) acc = fmaf(to_f32(Br[j]), ss[q * R + j], acc);
+        }
+        T* yp = y + (size_t)(t0 + q) * h_out + o;
+        *yp = from_f32<T>(to_f32(*yp) + acc);
+    }
+}
+
+// ---- CUDA-core base GEMM, optional fused expand ---------------------------------------------
+// 64 tokens x 64 outputs per CTA, 256 threads with 4 x 4 outputs each, K-chunks of 16.
+template <typename T>
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(PoolView pool, SegView seg, const T* __restrict__ W, const T* __restrict__ x,
+                 const float* __restrict__ s_in, T* __restrict__ y, int fuse_lora) {
+    __shared__ float xs[16][65];
+    __shared__ float ws[16][65];
+    pdl_wait();
+    pdl_trigger();
+    if (*seg.status != LORA_OK) return;
+    const int n = seg.n, h_in = pool.h_in, h_out = pool.h_out, R = pool.R;
+    const int t0 = blockIdx.y * 64, o0 = blockIdx.x * 64;
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < h_in; k0 += 16) {
+        for (int e = tid; e < 64 * 16; e += 256) {
+            const int r = e >> 4, kk = e & 15;
+            const int t = t0 + r, o = o0 + r, k = k0 + kk;
+            xs[kk][r] = (t < n && k < h_in) ? to_f32(x[(size_t)t * h_in + k]) : 0.f;
+            ws[kk][r] = (o < h_out && k < h_in) ? to_f32(W[(size_t)o * h_in + k]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty + 16 * i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) b[i] = ws[kk][tx + 16 * i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(a[i], b[jj], acc[i][jj]);
+        }
+        __syncthreads();
+    }
+    const T* B = static_cast<const T*>(pool.B);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty + 16 * i;
+        if (t >= n) continue;
+        const int s = fuse_lora ? seg.idx[t] : -1;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int o = o0 + tx + 16 * jj;
+            if (o >= h_out) continue;
+            float v = acc[i][jj];
+            if (s >= 0) {
+                const T* Br = B + ((size_t)s * h_out + o) * R;
+                const float* sr = s_in + (size_t)t * R;
+                float l = 0.f;
+                for (int j = 0; j < R; ++j) l = fmaf(sr[j], to_f32(Br[j]), l);
+                v += l;
+            }
+            y[(size_t)t * h_out + o] = from_f32<T>(v);
+        }
+    }
+}
+
+// ---- host launchers ----------------------------------------------------------------------------
+
+template <typename T>
+static int launch_shrink_t(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st,
+                           bool tiled) {
+    const T* xp = static_cast<const T*>(x);
+    if (!tiled) {
+        const int RG = (pv.R % 8 == 0) ? 8 : 1;
+        const long warps = (long)sv.n * (pv.R / RG);
+        const int blocks = (int)((warps + 7) / 8);
+        if (blocks == 0) return LORA_OK;
+        void* args[] = {(void*)&pv, (void*)&sv, (void*)&xp, (void*)&s_out};
+        const void* fn = RG == 8 ? (const void*)shrink_warp_kernel<T, 8> : (const void*)shrink_warp_kernel<T, 1>;
+        LORA_CUDA_TRY(launch_pdl(fn, dim3(blocks), dim3(256), 0, st, args));
+        return LORA_OK;
+    }
+    const int max_tiles = (sv.n + kShrTT - 1) / kShrTT + std::min(sv.n, pv.S + 1);
+    if (max_tiles == 0) return LORA_OK;
+    const size_t smem = sizeof(float) * (kShrTT + pv.R) * (kShrKC + 1);
+    static bool attr = false;
+    if (!attr) {
+        LORA_CUDA_TRY(cudaFuncSetAttribute(shrink_tiled_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)(sizeof(float) * (kShrTT + kMaxRank) * (kShrKC + 1))));
+        attr = true;
+    }
+    void* args[] = {(void*)&pv, (void*)&sv, (void*)&xp, (void*)&s_out};
+    LORA_CUDA_TRY(launch_pdl((const void*)shrink_tiled_kernel<T>, dim3(max_tiles), dim3(256), smem, st, args));
+    return LORA_OK;
+}
+
+int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled) {
+    switch (pv.dtype) {
+        case LORA_F32: return launch_shrink_t<float>(pv, sv, x, s_out, st, tiled);
+        case LORA_F16: return launch_shrink_t<__half>(pv, sv, x, s_out, st, tiled);
+        default: return launch_shrink_t<__nv_bfloat16>(pv, sv, x, s_out, st, tiled);
+    }
+}
+
+template <typename T>
+static int launch_expand_t(const PoolView& pv, const SegView& sv, const float* s_in, void* y, cudaStream_t st) {
+    if (sv.n == 0) return LORA_OK;
+    T* yp = static_cast<T*>(y);
+    const dim3 grid((pv.h_out + 255) / 256, (sv.n + kExpTT - 1) / kExpTT);
+    const size_t smem = sizeof(float) * kExpTT * pv.R;
+    void* args[] = {(void*)&pv, (void*)&sv, (void*)&s_in, (void*)&yp};
+    LORA_CUDA_TRY(launch_pdl((const void*)expand_kernel<T>, grid, dim3(256), smem, st, args));
+    return LORA_OK;
+}
+
+int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, void* y, cudaStream_t st) {
+    switch (pv.dtype) {
+        case LORA_F32: return launch_expand_t<float>(pv, sv, s_in, y, st);
+        case LORA_F16: return launch_expand_t<__half>(pv, sv, s_in, y, st);
+        default: return launch_expand_t<__nv_bfloat16>(pv, sv, s_in, y, st);
+    }
+}
+
+template <typename T>
+static int launch_gemm_simt_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
+                              void* y, bool fuse, cudaStream_t st) {
+    if (sv.n == 0) return LORA_OK;
+    const T* Wp = static_cast<const T*>(W);
+    const T* xp = static_cast<const T*>(x);
+    T* yp = static_cast<T*>(y);
+    int f = fuse ? 1 : 0;
+    const dim3 grid((pv.h_out + 63) / 64, (sv.n + 63) / 64);
+    void* args[] = {(void*)&pv, (void*)&sv, (void*)&Wp, (void*)&xp, (void*)&s_in, (void*)&yp, (void*)&f};
+    LORA_CUDA_TRY(launch_pdl((const void*)gemm_simt_kernel<T>, grid, dim3(256), 0, st, args));
+    return LORA_OK;
+}
+
+int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
+                     bool fuse, cudaStream_t st) {
+    switch (pv.dtype) {
+        case LORA_F32: return launch_gemm_simt_t<float>(pv, sv, W, x, s_in, y, fuse, st);
+        case LORA_F16: return launch_gemm_simt_t<__half>(pv, sv, W, x, s_in, y, fuse, st);
+        default: return launch_gemm_simt_t<__nv_bfloat16>(pv, sv, W, x, s_in, y, fuse, st);
+    }
+}
+
+}  // namespace lora

@@ -1,0 +1,187 @@
+/*
+ * lora.h -- C ABI of the GB300 (sm_103a) multi-LoRA segmented linear.
+ *
+ * The library computes, for a batch of n tokens that each name one adapter slot,
+ *
+ *     y[t,:] = x[t,:] W^T + (alpha_s / r_s) (x[t,:] A_s^T) B_s^T,   s = idx[t],
+ *
+ * with no LoRA term when idx[t] == -1, over a pool of adapters that lives in device
+ * memory with every rank zero-padded to a common r_max.
+ *
+ * Sources (web pages on multi-LoRA serving):
+ *  - "LLM 多 LoRA 推理服务工程 2026：从热插拔到租户编排" (blog.lonae.com):
+ *      the adapter execution unit (LoRA A/B applied onto the base hidden state, as a
+ *      fused kernel or as a separate residual kernel); the two-level bucketing of a
+ *      batch (request level, then adapter level); zero-padding low-rank adapters to
+ *      the high rank; the adapter storage pool with hot adapters resident in HBM.
+ *  - "Multi-LoRA 在线服务隔离：适配器身份、显存配额与跨租户防串用" (ai.codenodex.com),
+ *      section "请求身份决定适配器，而非客户端参数": a mixed-adapter batch keeps a
+ *      per-request index map; authorisation is default-deny and a missing mapping is
+ *      an explicit error, never a fallback to another adapter.
+ *  - xpshop.cn article 492 (on-prem multi-LoRA case study), section 三: over-quota
+ *      mounts are refused, base/adapter mismatches are refused at mount time, routing
+ *      default "base_only", routing resolved once at request entry.
+ *
+ * Conventions shared by every entry point:
+ *  - Ownership: the caller owns every buffer.  The library never allocates device
+ *    memory; pools and workspaces are carved out of caller memory.  Handles
+ *    (lora_pool_t) are small host structs owned by the library.
+ *  - Pointers named *_dev are device pointers; everything else is host memory.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call that touches the device only enqueues work on that stream
+ *    and returns without synchronising, except lora_segment_status.
+ *  - Layouts are row-major and densely packed: x [n, h_in], W [h_out, h_in] (the
+ *    nn.Linear layout), y [n, h_out], adapter A [rank, h_in], adapter B [h_out, rank].
+ *    x, W, y, A and B share the pool's dtype.
+ *  - Errors: a negative lora_status; lora_last_error() returns a message for the
+ *    calling thread.  Argument errors are detected on the host before anything is
+ *    enqueued.  Data-dependent errors (an idx out of range or naming an empty slot)
+ *    are detected on the device: the segment builder sets its status word to
+ *    LORA_EIDX and lora_linear_fwd then leaves y unwritten -- there is no fallback
+ *    to base-only output or to another adapter.
+ *  - Thread safety: calls on different pools are independent; calls on one pool must
+ *    not run concurrently from several host threads.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LORA_F32 = 0,  /* float32: CUDA-core path */
+    LORA_F16 = 1,  /* IEEE half: tcgen05 tensor-core path, fp32 accumulation */
+    LORA_BF16 = 2  /* bfloat16: tcgen05 tensor-core path, fp32 accumulation */
+} lora_dtype;
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_EINVAL = -1,   /* bad argument (null pointer, bad size, bad dtype, misalignment) */
+    LORA_ESLOT = -2,    /* slot index out of range */
+    LORA_EBUSY = -3,    /* slot already holds an adapter */
+    LORA_ERANK = -4,    /* rank < 1 or rank > r_max */
+    LORA_ENOSPACE = -5, /* caller buffer or workspace too small */
+    LORA_EIDX = -6,     /* (device) idx outside [-1, n_slots) or naming an empty slot */
+    LORA_ECUDA = -7,    /* a CUDA runtime call failed */
+    LORA_EUNSUP = -8,   /* shape/dtype combination this build does not support */
+    LORA_ETIMEOUT = -9  /* (device) a pipeline wait exceeded its time limit; output invalid */
+} lora_status;
+
+typedef enum {
+    LORA_VARIANT_AUTO = 0,     /* the library's measured policy picks */
+    LORA_VARIANT_FUSED = 1,    /* expand fused into the base GEMM epilogue */
+    LORA_VARIANT_SEPARATE = 2, /* base GEMM, then a separate residual expand kernel */
+    LORA_VARIANT_CUDA_CORE = 3 /* diagnostic: CUDA-core base GEMM with fused expand, no tensor cores */
+} lora_variant;
+
+/* Shape of one pool.  One pool serves one linear layer (one base weight W). */
+typedef struct {
+    int32_t h_in;     /* input features  (>= 1; multiple of 8 for 16-bit dtypes) */
+    int32_t h_out;    /* output features (>= 1; multiple of 8 for 16-bit dtypes) */
+    int32_t r_max;    /* padded rank, 1..256 (multiple of 8 for 16-bit dtypes) */
+    int32_t n_slots;  /* adapter slots, 1..2048 */
+    int32_t dtype;    /* lora_dtype */
+} lora_pool_desc;
+
+typedef struct lora_pool* lora_pool_t;
+
+/* Output of lora_segment: device pointers into the caller's segment workspace.
+ * Sorted order = stable sort of token positions by idx, with -1 as the smallest key.
+ *   perm_dev[j]       original position of the j-th token in sorted order     [n]
+ *   seg_start_dev[i]  first sorted position of segment i; seg_start[nseg] = n  [n_slots+2]
+ *   seg_slot_dev[i]   slot of segment i (-1 for the base-only run)            [n_slots+1]
+ *   nseg_dev          number of segments                                      [1]
+ *   status_dev        LORA_OK or LORA_EIDX                                    [1]
+ *   idx_dev           copy of the batch's idx (original order)               [n]
+ * Segments are rebuilt once per batch and reused by every linear layer that runs
+ * over that batch, as long as the workspace stays alive and unmodified. */
+typedef struct {
+    int32_t* perm_dev;
+    int32_t* seg_start_dev;
+    int32_t* seg_slot_dev;
+    int32_t* nseg_dev;
+    int32_t* status_dev;
+    int32_t* idx_dev;
+    int32_t n_tokens;
+    int32_t n_slots;
+} lora_segments;
+
+/* ---- adapter pool (device-resident slot table + zero-padded A/B slabs) ---------------
+ * Layout inside the caller's buffer (all offsets 256-byte aligned):
+ *   slot table  n_slots x {int32 rank, int32 state, float scale, int32 reserved}
+ *   A slab      [n_slots, r_max, h_in]   rows >= rank are zero
+ *   B slab      [n_slots, h_out, r_max]  columns >= rank are zero
+ * scale = alpha / rank with the adapter's true rank. */
+
+/* Bytes a pool with this shape needs.  LORA_EINVAL on a bad shape. */
+int lora_pool_bytes(const lora_pool_desc* desc, size_t* bytes);
+
+/* Create a pool inside dev_mem (device, >= lora_pool_bytes, 256-byte aligned).
+ * Enqueues one memset on `stream` that empties every slot and zeroes both slabs.
+ * The handle is valid until lora_pool_destroy; dev_mem must outlive it. */
+int lora_pool_create(const lora_pool_desc* desc, void* dev_mem, size_t bytes, void* stream,
+                     lora_pool_t* out);
+
+/* Free the host handle.  The caller's device memory is not touched. */
+int lora_pool_destroy(lora_pool_t pool);
+
+/* Mount an adapter into an empty slot: copy A_dev [rank, h_in] and B_dev [h_out, rank]
+ * (device pointers, pool dtype, row-major) into the slot with zero padding up to r_max
+ * and mark it ready with scale alpha/rank.  Stream-ordered.  Errors: LORA_ESLOT (slot
+ * out of range), LORA_ERANK (rank < 1 or > r_max), LORA_EBUSY (slot already mounted:
+ * hot swap must unmount first), LORA_EINVAL (null pointers). */
+int lora_pool_load_slot(lora_pool_t pool, int slot, const void* A_dev, const void* B_dev, int rank,
+                        float alpha, void* stream);
+
+/* Mark a slot empty again (stream-ordered).  Work already enqueued that reads the slot
+ * is unaffected; batches segmented afterwards that name it fail with LORA_EIDX. */
+int lora_pool_unload_slot(lora_pool_t pool, int slot, void* stream);
+
+/* ---- segment builder ------------------------------------------------------------------ */
+
+/* Workspace bytes lora_segment needs for n_tokens tokens over n_slots slots. */
+int lora_segment_workspace_bytes(int n_tokens, int n_slots, size_t* bytes);
+
+/* Validate idx_dev [n_tokens] (device int32) against the pool's slot table and build
+ * the stable segments into ws_dev (device, >= lora_segment_workspace_bytes, 256-byte
+ * aligned).  One kernel, no host synchronisation.  n_tokens may be 0.  If any idx is
+ * out of range or names an empty slot, *status_dev = LORA_EIDX and nseg = 0. */
+int lora_segment(const int32_t* idx_dev, int n_tokens, lora_pool_t pool, void* ws_dev, size_t ws_bytes,
+                 lora_segments* out, void* stream);
+
+/* Synchronise `stream` and read the device status word (debug/test helper). */
+int lora_segment_status(const lora_segments* seg, void* stream, int* status);
+
+/* ---- LoRA-augmented linear --------------------------------------------------------------- */
+
+/* Workspace bytes lora_linear_fwd needs for n_tokens tokens on this pool. */
+int lora_linear_workspace_bytes(lora_pool_t pool, int n_tokens, size_t* bytes);
+
+/* y_dev = x_dev W_dev^T + per-token LoRA term (see top of file).
+ *   W_dev [h_out, h_in], x_dev [n, h_in], y_dev [n, h_out]: device, pool dtype, 16-byte
+ *   aligned for 16-bit dtypes; n = seg->n_tokens; seg from lora_segment on this pool's
+ *   slot count; variant a lora_variant; ws_dev device workspace of
+ *   >= lora_linear_workspace_bytes, 256-byte aligned, zero-filled before its first use
+ *   (every call leaves its counter region zeroed again).
+ * If seg's status word is not LORA_OK the kernels leave y untouched. */
+int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
+                    const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Which variant LORA_VARIANT_AUTO picks for n_tokens on this pool (1 or 2). */
+int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* lora_last_error(void);
+
+/* Number of kernels this library has launched in this process (instrumentation). */
+uint64_t lora_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GB300_H */

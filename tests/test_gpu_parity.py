@@ -1,0 +1,284 @@
+"""GPU parity of the CUDA path (through the C ABI) against the float64 CPU oracle.
+
+Bars: segment outputs bit-exact; floats elementwise |y - y_ref| <= 1e-2 + 1e-2 |y_ref|.
+Because that bar is loose next to the LoRA term at the workloads' scales, every config is
+also run with W = 0 (y is then the LoRA term alone, compared against a bar scaled by the
+largest |y_ref|), and a negative control (outputs compared with the oracle of a shuffled
+idx) must fail.
+"""
+import numpy as np
+import pytest
+import torch
+
+from adapter_gemm_segment_gb300 import workloads as wl
+from oracle import lora_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+# ------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------
+
+def make_pool(ags, case, n_slots=None, load=True):
+    ad = case.adapters
+    S = n_slots or ad.n_slots
+    pool = ags.LoraPool(case.h_in, case.h_out, ad.r_max, S, case.dtype, DEV)
+    if load:
+        for s in range(ad.n_slots):
+            pool.load_slot(s, ad.A[s].to(DEV), ad.B[s].to(DEV), ad.alphas[s])
+    return pool
+
+
+def run(ags, case, variant=0, W=None, idx=None, pool=None):
+    pool = pool or make_pool(ags, case)
+    idx = case.idx if idx is None else idx
+    seg = pool.segment(idx.to(DEV))
+    Wd = (case.W if W is None else W).to(DEV)
+    y = pool.linear(Wd, case.x.to(DEV), seg, variant=variant)
+    torch.cuda.synchronize()
+    return y.cpu(), pool, seg
+
+
+def assert_parity(y, y_ref, what=""):
+    ok = O.within_tolerance(y, y_ref)
+    bad = np.count_nonzero(~ok)
+    if bad:
+        y64 = y.double().numpy()
+        i = np.unravel_index(np.argmax(np.abs(y64 - y_ref)), y_ref.shape)
+        pytest.fail(f"{what}: {bad}/{ok.size} elements outside tolerance; worst at {i}: got {y64[i]}, want {y_ref[i]}")
+
+
+def assert_lora_only_parity(y, y_ref, what=""):
+    y64 = y.double().numpy()
+    bound = 1e-2 * np.abs(y_ref).max() + 1e-2 * np.abs(y_ref)
+    bad = np.count_nonzero(np.abs(y64 - y_ref) > bound)
+    assert bad == 0, f"{what}: {bad} elements of the LoRA-only output outside tolerance"
+
+
+def seg_arrays(ags, seg):
+    return {k: v.cpu().numpy() for k, v in ags.segment_arrays(seg).items()}
+
+
+def check_segments(ags, seg, idx, S):
+    got = seg_arrays(ags, seg)
+    perm, ss, sl, nseg = O.segments(np.asarray(idx), S)
+    assert int(got["status"][0]) == 0
+    assert int(got["nseg"][0]) == nseg
+    assert np.array_equal(got["perm"], perm)
+    assert np.array_equal(got["seg_start"][:nseg + 1], ss)
+    assert np.array_equal(got["seg_slot"][:nseg], sl)
+    assert np.array_equal(got["idx"], np.asarray(idx))
+
+
+# ------------------------------------------------------------------------------------------
+# pool
+# ------------------------------------------------------------------------------------------
+
+def test_pool_load_is_exact_zero_pad(lib):
+    case = wl.random_case(1, 8, 64, 48, [3, 8, 1], r_max=16, dtype=torch.float16)
+    pool = make_pool(lib, case, n_slots=5)
+    torch.cuda.synchronize()
+    S, R = 5, 16
+    mem = pool.mem
+    table = mem[:S * 16].view(torch.int32).view(S, 4).cpu().numpy()
+    scale = mem[:S * 16].view(torch.float32).view(S, 4)[:, 2].cpu().numpy()
+    ad = case.adapters
+    ref = O.pad_pool(ad.A, ad.B, ad.ranks, ad.alphas, R, 64, 48, n_slots=S)
+    assert table[:, 0].tolist() == [3, 8, 1, 0, 0]
+    assert table[:, 1].tolist() == [1, 1, 1, 0, 0]
+    assert np.array_equal(scale, ref.scale.astype(np.float32))
+    a_off = 256
+    A = mem[a_off:a_off + S * R * 64 * 2].view(torch.float16).view(S, R, 64).cpu().double().numpy()
+    b_off = a_off + S * R * 64 * 2
+    b_off = (b_off + 255) // 256 * 256
+    B = mem[b_off:b_off + S * 48 * R * 2].view(torch.float16).view(S, 48, R).cpu().double().numpy()
+    assert np.array_equal(A, ref.A) and np.array_equal(B, ref.B)
+
+
+def test_pool_mount_errors(lib):
+    case = wl.random_case(2, 4, 64, 64, [8, 8], r_max=8, dtype=torch.float16)
+    pool = make_pool(lib, case)
+    A, B = case.adapters.A[0].to(DEV), case.adapters.B[0].to(DEV)
+    with pytest.raises(lib.LoraError) as e:
+        pool.load_slot(0, A, B, 16.0)
+    assert e.value.code == lib.LORA_EBUSY
+    with pytest.raises(lib.LoraError) as e:
+        pool.load_slot(2, A, B, 16.0)
+    assert e.value.code == lib.LORA_ESLOT
+    big = torch.zeros(9, 64, dtype=torch.float16, device=DEV)
+    with pytest.raises(lib.LoraError) as e:
+        lib.lora_pool_load_slot(pool.handle, 1, big, torch.zeros(64, 9, dtype=torch.float16, device=DEV), 9, 1.0)
+    assert e.value.code == lib.LORA_ERANK
+    pool.unload_slot(0)
+    pool.load_slot(0, A, B, 16.0)  # unmount, then mount again
+
+
+# ------------------------------------------------------------------------------------------
+# segments
+# ------------------------------------------------------------------------------------------
+
+SEG_CASES = {
+    "all_base": (np.full(37, -1), 4),
+    "one_slot": (np.full(50, 2), 4),
+    "single_token": (np.array([3]), 4),
+    "every_slot": (np.arange(100)[::-1].copy(), 100),
+    "zipf_decode_64": (wl.draw_zipf_idx(np.random.default_rng(1), 64, 100, 0.1), 100),
+    "uniform_1500": (np.random.default_rng(2).integers(-1, 7, 1500), 7),
+    "prefill_16384": (np.repeat(wl.draw_zipf_idx(np.random.default_rng(3), 32, 100), 512), 100),
+    "max_slots": (np.random.default_rng(4).integers(-1, 2048, 5000), 2048),
+    "long_run_3000": (np.concatenate([np.full(3000, 5), np.full(10, -1), np.full(1030, 1)]), 8),
+}
+
+
+@pytest.mark.parametrize("name", list(SEG_CASES))
+def test_segments_bitexact(lib, name):
+    idx, S = SEG_CASES[name]
+    idx = np.asarray(idx, np.int32)
+    pool = lib.LoraPool(64, 64, 8, S, torch.float16, DEV)
+    A = torch.zeros(8, 64, dtype=torch.float16, device=DEV)
+    B = torch.zeros(64, 8, dtype=torch.float16, device=DEV)
+    for s in sorted(set(idx.tolist()) - {-1}):
+        pool.load_slot(s, A, B, 8.0)
+    seg = pool.segment(torch.from_numpy(idx).to(DEV))
+    torch.cuda.synchronize()
+    check_segments(lib, seg, idx, S)
+
+
+def test_segments_empty_batch(lib):
+    pool = lib.LoraPool(64, 64, 8, 4, torch.float16, DEV)
+    seg = pool.segment(torch.zeros(0, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    got = seg_arrays(lib, seg)
+    assert int(got["nseg"][0]) == 0 and int(got["seg_start"][0]) == 0 and int(got["status"][0]) == 0
+    y = pool.linear(torch.zeros(64, 64, dtype=torch.float16, device=DEV),
+                    torch.zeros(0, 64, dtype=torch.float16, device=DEV), seg)
+    assert y.shape == (0, 64)
+
+
+@pytest.mark.parametrize("bad", ["out_of_range", "below_minus_one", "unmounted"])
+@pytest.mark.parametrize("n", [16, 300])
+def test_invalid_idx_is_an_error_and_y_untouched(lib, bad, n):
+    case = wl.random_case(3, n, 128, 128, [8, 8, 8], r_max=8, dtype=torch.float16)
+    pool = make_pool(lib, case, n_slots=4)  # slot 3 stays empty
+    idx = case.idx.clone()
+    idx[n // 2] = {"out_of_range": 4, "below_minus_one": -2, "unmounted": 3}[bad]
+    seg = pool.segment(idx.to(DEV))
+    assert lib.lora_segment_status(seg) == lib.LORA_EIDX
+    y = torch.full((n, 128), 7.0, dtype=torch.float16, device=DEV)
+    for variant in (1, 2, 3):
+        pool.linear(case.W.to(DEV), case.x.to(DEV), seg, variant=variant, y=y)
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all()), "y was written although the batch names an invalid slot"
+
+
+# ------------------------------------------------------------------------------------------
+# linear: small cases, all variants
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+def test_tiny_fp32(lib, variant):
+    case = wl.tiny()
+    y, pool, seg = run(lib, case, variant)
+    torch.cuda.synchronize()
+    check_segments(lib, seg, case.idx.numpy(), 4)
+    assert_parity(y, O.lora_linear_case(case), f"tiny variant {variant}")
+    y0, _, _ = run(lib, case, variant, W=torch.zeros_like(case.W))
+    pool0 = O.pool_of_case(case)
+    assert_lora_only_parity(y0, O.lora_linear(case.x, torch.zeros_like(case.W), pool0, case.idx.numpy()))
+
+
+SMALL = [
+    # (seed, n, h_in, h_out, ranks, r_max, dtype)
+    (10, 16, 256, 256, [8, 8, 8], 8, torch.float16),
+    (11, 1, 128, 256, [8], 8, torch.float16),
+    (12, 17, 200, 136, [8, 16], 16, torch.bfloat16),
+    (13, 64, 512, 384, [8, 8, 16, 64, 64, 16], 64, torch.float16),
+    (14, 255, 136, 264, [16, 8, 4, 1], 16, torch.bfloat16),
+    (15, 256, 256, 128, [8] * 10, 8, torch.float16),
+    (16, 257, 256, 520, [16, 16, 16], 16, torch.bfloat16),
+    (17, 300, 512, 256, [16, 3, 16], 16, torch.bfloat16),
+    (18, 700, 136, 392, [8, 8], 8, torch.float16),
+    (19, 129, 4104, 64, [8, 8], 8, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("variant", [3, 1, 2])
+@pytest.mark.parametrize("spec", SMALL, ids=[f"n{s[1]}_{s[2]}x{s[3]}_R{s[5]}" for s in SMALL])
+def test_small_cases(lib, spec, variant):
+    seed, n, h_in, h_out, ranks, r_max, dtype = spec
+    case = wl.random_case(seed, n, h_in, h_out, ranks, r_max=r_max, dtype=dtype, p_base=0.15)
+    y, pool, seg = run(lib, case, variant)
+    check_segments(lib, seg, case.idx.numpy(), len(ranks))
+    assert_parity(y, O.lora_linear_case(case), f"{case.name} variant {variant}")
+    y0, _, _ = run(lib, case, variant, W=torch.zeros_like(case.W), pool=pool)
+    assert_lora_only_parity(y0, O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case),
+                                              case.idx.numpy()), f"{case.name} W=0 variant {variant}")
+
+
+def test_repeated_calls_are_bit_identical(lib):
+    case = wl.decode_q_proj(n=48, h=1024)
+    pool = make_pool(lib, case)
+    seg = pool.segment(case.idx.to(DEV))
+    W, x = case.W.to(DEV), case.x.to(DEV)
+    ys = [pool.linear(W, x, seg, variant=1).clone() for _ in range(4)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
+# ------------------------------------------------------------------------------------------
+# the five workloads
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_decode_q_proj_full(lib, variant):
+    case = wl.decode_q_proj()
+    y, pool, seg = run(lib, case, variant)
+    check_segments(lib, seg, case.idx.numpy(), 100)
+    y_ref = O.lora_linear_case(case)
+    assert_parity(y, y_ref, f"decode q_proj variant {variant}")
+    y0, _, _ = run(lib, case, variant, W=torch.zeros_like(case.W), pool=pool)
+    y0_ref = O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case), case.idx.numpy())
+    assert_lora_only_parity(y0, y0_ref, "decode q_proj W=0")
+    # negative control: the LoRA-only output must not match the oracle of a shuffled routing
+    idx_sh = case.idx.numpy()[np.random.default_rng(0).permutation(case.n)]
+    y0_wrong = O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case), idx_sh)
+    bound = 1e-2 * np.abs(y0_wrong).max() + 1e-2 * np.abs(y0_wrong)
+    assert np.count_nonzero(np.abs(y0.double().numpy() - y0_wrong) > bound) > 0
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64])
+def test_mixed_rank_sweep(lib, n):
+    case = wl.mixed_rank(n)
+    for variant in (1, 2):
+        y, pool, seg = run(lib, case, variant)
+        assert_parity(y, O.lora_linear_case(case), f"mixed rank n={n} variant {variant}")
+        y0, _, _ = run(lib, case, variant, W=torch.zeros_like(case.W), pool=pool)
+        y0_ref = O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case), case.idx.numpy())
+        assert_lora_only_parity(y0, y0_ref, f"mixed rank n={n} W=0 variant {variant}")
+
+
+def test_prefill_full_sampled(lib):
+    cases = wl.prefill()
+    rows = np.sort(np.random.default_rng(7).choice(16384, 192, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, 127, 128, 511, 512, 16383]]))
+    for case in cases:
+        for variant in (1, 2):
+            y, pool, seg = run(lib, case, variant)
+            if variant == 1:
+                check_segments(lib, seg, case.idx.numpy(), 100)
+            assert_parity(y[rows], O.lora_linear_case(case, rows=rows), f"{case.name} variant {variant}")
+        y0, _, _ = run(lib, case, 1, W=torch.zeros_like(case.W), pool=pool)
+        y0_ref = O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case), case.idx.numpy(), rows=rows)
+        assert_lora_only_parity(y0[rows], y0_ref, f"{case.name} W=0")
+
+
+def test_full_layer_sampled(lib):
+    cases = wl.full_layer(layer=0)
+    rows = np.array([0, 1, 63, 64, 100, 200, 254, 255])
+    for case in cases:
+        y, pool, seg = run(lib, case, 0)
+        assert_parity(y[rows], O.lora_linear_case(case, rows=rows), case.name)
