@@ -12,9 +12,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def ags():
-    from adapter_gemm_segment_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__.build()
     import adapter_gemm_segment_gb300 as m
 
     return m
