@@ -33,6 +33,7 @@ EXPORTED = (
     "lora_pool_bytes", "lora_pool_create", "lora_pool_destroy", "lora_pool_load_slot", "lora_pool_unload_slot",
     "lora_segment_workspace_bytes", "lora_segment", "lora_segment_status", "lora_linear_workspace_bytes",
     "lora_linear_fwd", "lora_linear_policy", "lora_last_error", "lora_kernel_launch_count",
+    "lora_set_timing_events",
 )
 
 
@@ -72,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "lora_linear_workspace_bytes": [vp, i32, P(sz)],
         "lora_linear_fwd": [vp, vp, vp, vp, P(lora_segments), i32, vp, sz, vp],
         "lora_linear_policy": [vp, i32, P(i32)],
+        "lora_set_timing_events": [vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -93,6 +95,15 @@ def lora_last_error() -> str:
 
 def lora_kernel_launch_count() -> int:
     return int(_lib.lora_kernel_launch_count())
+
+
+def lora_set_timing_events(before_shrink=None, before_gemm=None, after_gemm=None) -> None:
+    """Events (torch.cuda.Event, already recorded once so they exist) recorded around the
+    kernels of every following lora_linear_fwd; call with no arguments to disable."""
+    def h(e):
+        return ctypes.c_void_p(0 if e is None else e.cuda_event)
+
+    _check(_lib.lora_set_timing_events(h(before_shrink), h(before_gemm), h(after_gemm)))
 
 
 def _check(rc: int) -> None:

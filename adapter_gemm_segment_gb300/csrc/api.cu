@@ -55,6 +55,13 @@ int num_sms() {
     return sms;
 }
 
+// Benchmark instrumentation: events recorded around the kernels of lora_linear_fwd.
+static cudaEvent_t g_ev_before_shrink = nullptr, g_ev_before_gemm = nullptr, g_ev_after_gemm = nullptr;
+
+static void record_if(cudaEvent_t e, cudaStream_t st) {
+    if (e) cudaEventRecord(e, st);
+}
+
 // Fused expand from this many tokens up; below it the separate residual kernel.
 constexpr int kFusedMinTokens = 1;
 constexpr int kVariantCudaCore = LORA_VARIANT_CUDA_CORE;
@@ -91,6 +98,13 @@ extern "C" {
 const char* lora_last_error(void) { return g_err; }
 
 uint64_t lora_kernel_launch_count(void) { return g_launches.load(); }
+
+int lora_set_timing_events(void* before_shrink, void* before_gemm, void* after_gemm) {
+    g_ev_before_shrink = static_cast<cudaEvent_t>(before_shrink);
+    g_ev_before_gemm = static_cast<cudaEvent_t>(before_gemm);
+    g_ev_after_gemm = static_cast<cudaEvent_t>(after_gemm);
+    return LORA_OK;
+}
 
 int lora_linear_workspace_bytes(lora_pool_t pool, int n_tokens, size_t* bytes) {
     if (!pool || !bytes) return set_error(LORA_EINVAL, "pool/bytes is NULL");
@@ -134,8 +148,10 @@ int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void
 
     const bool tc = variant != kVariantCudaCore && tc_supported(pv, n);
     const bool fused = variant != LORA_VARIANT_SEPARATE;
+    record_if(g_ev_before_shrink, st);
     int rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256);
     if (rc) return rc;
+    record_if(g_ev_before_gemm, st);
     if (tc) {
         TcWorkspace tw;
         tw.partials = reinterpret_cast<float*>(w + L.part_off);
@@ -147,6 +163,7 @@ int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void
         rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, st);
     }
     if (rc) return rc;
+    record_if(g_ev_after_gemm, st);
     if (!fused) {
         rc = launch_expand(pv, sv, s_buf, y_dev, st);
         if (rc) return rc;

@@ -180,6 +180,13 @@ const char* lora_last_error(void);
 /* Number of kernels this library has launched in this process (instrumentation). */
 uint64_t lora_kernel_launch_count(void);
 
+/* Timing instrumentation for benchmarks: while set (non-NULL cudaEvent_t handles passed as
+ * void*), every lora_linear_fwd records before_shrink on its stream before the shrink
+ * kernel, before_gemm between the shrink and the base-GEMM kernel, and after_gemm after the
+ * base-GEMM kernel.  The records serialise those kernels (no launch overlap), so the
+ * intervals are per-kernel durations.  Process-wide, not thread-safe; NULLs disable. */
+int lora_set_timing_events(void* before_shrink, void* before_gemm, void* after_gemm);
+
 #ifdef __cplusplus
 }
 #endif
