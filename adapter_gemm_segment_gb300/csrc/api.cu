@@ -59,7 +59,15 @@ int num_sms() {
 static cudaEvent_t g_ev_before_shrink = nullptr, g_ev_before_gemm = nullptr, g_ev_after_gemm = nullptr;
 
 static void record_if(cudaEvent_t e, cudaStream_t st) {
-    if (e) cudaEventRecord(e, st);
+    if (!e) return;
+    // Under stream capture a plain record only tracks dependencies; an external record node
+    // is what re-records the event at every graph replay.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, st);
 }
 
 // Fused expand from this many tokens up; below it the separate residual kernel.
