@@ -74,26 +74,15 @@ static void record_if(cudaEvent_t e, cudaStream_t st) {
 constexpr int kFusedMinTokens = 1;
 constexpr int kVariantCudaCore = LORA_VARIANT_CUDA_CORE;
 
+// Linear workspace: the shrink output s [n, r_max] float32 (alpha/r folded in).
 struct LinWsLayout {
-    size_t s_off, cnt_off, part_off, total;
-    int counters;
-    size_t partial_floats;
+    size_t s_off, total;
 };
 
 static LinWsLayout lin_layout(const PoolView& pv, int n) {
     LinWsLayout L;
-    size_t o = 0;
-    L.s_off = o;
-    o += align256(sizeof(float) * (size_t)(n > 0 ? n : 1) * pv.R);
-    int counters = 0;
-    const size_t pf = tc_workspace_floats(pv, n, &counters);
-    L.counters = counters;
-    L.partial_floats = pf;
-    L.cnt_off = o;
-    o += align256(sizeof(int32_t) * (size_t)(counters > 0 ? counters : 1));
-    L.part_off = o;
-    o += align256(sizeof(float) * (pf > 0 ? pf : 1));
-    L.total = o;
+    L.s_off = 0;
+    L.total = align256(sizeof(float) * (size_t)(n > 0 ? n : 1) * pv.R);
     return L;
 }
 
@@ -157,16 +146,15 @@ int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void
     const bool tc = variant != kVariantCudaCore && tc_supported(pv, n);
     const bool fused = variant != LORA_VARIANT_SEPARATE;
     record_if(g_ev_before_shrink, st);
-    int rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256);
+    int rc;
+    if (tc && n > 256 && shrink_tc_supported(pv))
+        rc = launch_shrink_tc(pv, sv, x_dev, s_buf, st);
+    else
+        rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256);
     if (rc) return rc;
     record_if(g_ev_before_gemm, st);
     if (tc) {
-        TcWorkspace tw;
-        tw.partials = reinterpret_cast<float*>(w + L.part_off);
-        tw.counters = reinterpret_cast<int32_t*>(w + L.cnt_off);
-        tw.partial_floats = L.partial_floats;
-        tw.counter_count = L.counters;
-        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, tw, st);
+        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, st);
     } else {
         rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, st);
     }

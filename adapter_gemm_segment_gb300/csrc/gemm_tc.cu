@@ -29,6 +29,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
+#include "tma_host.h"
 
 namespace lora {
 namespace tc {
@@ -48,8 +49,6 @@ struct DecodeArgs {
     SegView seg;
     const float* s_in;
     void* y;
-    float* partials;
-    int32_t* counters;
     int n, n_pad, kb_total, splits, kb_per_split, stages, tmem_cols, fuse, bf16;
 };
 
@@ -82,11 +81,14 @@ __device__ __forceinline__ float lora_term(const T* __restrict__ Brow, const flo
     return acc;
 }
 
-__device__ __forceinline__ void report_timeout(int32_t* status) { atomicExch(status, LORA_ETIMEOUT); }
-
 // ============================================================================================
-// decode: swap-AB + split-K
+// decode: swap-AB + split-K over a thread-block cluster
 // ============================================================================================
+// The `splits` CTAs that share one 128-feature tile form a cluster (cluster dims 1 x splits).
+// After its K range, every CTA parks its float32 partial tile [n_pad tokens][128 features] in
+// its own shared memory (the pipeline stages are free by then); after a cluster barrier CTA r
+// sums the partials of tokens [r*per, (r+1)*per) over the cluster through distributed shared
+// memory, adds the LoRA term of those tokens and writes y.  No global scratch, no atomics.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -101,7 +103,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     uint64_t* empty = full + stages;
     uint64_t* tmem_full = empty + stages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
-    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort, last CTA, go
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort, go, distinct count
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, split = blockIdx.y;
@@ -116,6 +118,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         mbar_init(tmem_full, 1);
         flags[0] = 0;
         flags[1] = 0;
+        flags[2] = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -155,7 +158,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 ++issued;
             }
             if (flags[0]) {  // aborted: let copies already in flight land before the CTA exits
-                report_timeout(a.seg.status);
+                report_timeout_status(a.seg.status);
                 for (int i = max(0, issued - stages); i < issued; ++i) {
                     const unsigned long long t0 = globaltimer();
                     while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
@@ -169,7 +172,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % stages;
                 if (!mbar_wait(&full[s], (i / stages) & 1, flags)) {
-                    report_timeout(a.seg.status);
+                    report_timeout_status(a.seg.status);
                     break;
                 }
                 tc_fence_after();
@@ -183,86 +186,156 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
             umma_commit(tmem_full);  // also on abort: fires once the issued MMAs have finished
         }
-    } else {
-        // ---- epilogue: warps 2..5, thread <-> output feature (TMEM lane) ----
-        const int q = warp & 3;
-        const int row = q * 32 + lane;
-        const int o = m_tile * BM + row;
-        const int h_out = a.pool.h_out, R = a.pool.R, n = a.n;
+    }
+
+    // ---- epilogue part 1 (warps 2..5): park the partial tile, stage this CTA's LoRA operands ----
+    const int et = threadIdx.x - 64;  // 0..127 in the epilogue warps
+    const int row = (warp & 3) * 32 + lane;
+    const int o = m_tile * BM + row;
+    const int h_out = a.pool.h_out, R = a.pool.R, n = a.n;
+    const int per = (a.n_pad + a.splits - 1) / a.splits;  // tokens reduced by each CTA
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int t0 = rank * per;
+    const int cnt = max(0, min(n, t0 + per) - t0);
+    float* P = reinterpret_cast<float*>(smem);                       // [n_pad][128]
+    int* slot_sm = reinterpret_cast<int*>(P + (size_t)a.n_pad * BM);  // [per]
+    int* dloc_sm = slot_sm + per;                                     // [per]
+    int* dlist = dloc_sm + per;                                       // [per]
+    int* fidx_sm = dlist + per;                                       // [per]
+    float* S_sm = reinterpret_cast<float*>(fidx_sm + per);            // [per][R]
+    float* Y_sm = S_sm + (size_t)per * R;                             // [per][128]
+    T* B_sm = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(Y_sm + (size_t)per * BM + 3) & ~uintptr_t(15));
+    const size_t b_cap_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(B_sm) - smem);
+    const int dcap = static_cast<int>(b_cap_bytes / ((size_t)BM * R * sizeof(T)));
+    if (warp >= 2) {
         const bool got = mbar_wait(tmem_full, 0, flags);
         tc_fence_after();
         pdl_wait();
         const int status = __ldcg(a.seg.status);
-        // one decision for all four epilogue warps (they meet at named barriers below)
         named_bar_sync(1, 128);
-        if (threadIdx.x == 64) flags[2] = (got && !flags[0] && status == LORA_OK) ? 1 : 0;
+        if (et == 0) flags[1] = (got && !flags[0] && status == LORA_OK && dcap >= 1) ? 1 : 0;
         named_bar_sync(1, 128);
-        if (flags[2]) {
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            const T* B = static_cast<const T*>(a.pool.B);
-            T* y = static_cast<T*>(a.y);
-            if (a.splits == 1) {
-                for (int c0 = 0; c0 < a.n_pad; c0 += 16) {
-                    uint32_t r[16];
-                    __syncwarp();
-                    tmem_ld16(taddr + c0, r);
-                    tmem_ld_wait();
-                    if (o < h_out) {
+        if (flags[1]) {
+            const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            for (int c0 = 0; c0 < a.n_pad; c0 += 16) {
+                uint32_t r[16];
+                __syncwarp();
+                tmem_ld16(taddr + c0, r);
+                tmem_ld_wait();
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int t = c0 + c;
-                            if (t < n) {
-                                float v = __uint_as_float(r[c]);
-                                if (a.fuse) {
-                                    const int s = __ldcg(a.seg.idx + t);
-                                    if (s >= 0)
-                                        v += lora_term<T>(B + ((size_t)s * h_out + o) * R, a.s_in + (size_t)t * R, R);
-                                }
-                                y[(size_t)t * h_out + o] = from_f32<T>(v);
-                            }
-                        }
-                    }
-                }
-            } else {
-                float* part = a.partials + (size_t)(m_tile * a.splits + split) * a.n_pad * BM;
-                for (int c0 = 0; c0 < a.n_pad; c0 += 16) {
-                    uint32_t r[16];
-                    __syncwarp();
-                    tmem_ld16(taddr + c0, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) __stcg(part + (size_t)(c0 + c) * BM + row, __uint_as_float(r[c]));
-                }
-                __threadfence();
+                for (int c = 0; c < 16; ++c) P[(c0 + c) * BM + row] = __uint_as_float(r[c]);
+            }
+            if (a.fuse) {
+                for (int q = et; q < cnt; q += 128) slot_sm[q] = __ldcg(a.seg.idx + t0 + q);
                 named_bar_sync(1, 128);
-                if (threadIdx.x == 64) {
-                    const int prev = atomicAdd(a.counters + m_tile, 1);
-                    flags[1] = (prev == a.splits - 1) ? 1 : 0;
+                // distinct slots of this CTA's tokens: dloc_sm[q] = index of token q's slot in dlist
+                for (int q = et; q < cnt; q += 128) {
+                    int first = -1;
+                    if (slot_sm[q] >= 0) {
+                        first = q;
+                        for (int q2 = 0; q2 < q; ++q2)
+                            if (slot_sm[q2] == slot_sm[q]) {
+                                first = q2;
+                                break;
+                            }
+                    }
+                    fidx_sm[q] = first;
+                }
+                int* wsum = reinterpret_cast<int*>(const_cast<int*>(flags)) + 4;  // 4 ints
+                int running = 0;
+                for (int c0 = 0; c0 < cnt; c0 += 128) {  // block-wide exclusive scan of "first occurrence"
+                    const int q = c0 + et;
+                    named_bar_sync(1, 128);
+                    const bool is_first = q < cnt && fidx_sm[q] == q;
+                    const unsigned bal = __ballot_sync(0xffffffffu, is_first);
+                    if (lane == 0) wsum[(et >> 5)] = __popc(bal);
+                    named_bar_sync(1, 128);
+                    int base = running;
+                    for (int w = 0; w < (et >> 5); ++w) base += wsum[w];
+                    if (is_first) {
+                        const int d = base + __popc(bal & ((1u << lane) - 1u));
+                        dloc_sm[q] = d;
+                        dlist[d] = slot_sm[q];
+                    }
+                    running += wsum[0] + wsum[1] + wsum[2] + wsum[3];
+                }
+                if (et == 0) flags[2] = running;
+                named_bar_sync(1, 128);
+                for (int q = et; q < cnt; q += 128) {
+                    const int f = fidx_sm[q];
+                    if (f != q) dloc_sm[q] = f >= 0 ? dloc_sm[f] : -1;
+                }
+                for (int e = et; e < cnt * R; e += 128) {
+                    const int q = e / R;
+                    S_sm[e] = slot_sm[q] >= 0 ? __ldcg(a.s_in + (size_t)(t0 + q) * R + (e % R)) : 0.f;
                 }
                 named_bar_sync(1, 128);
-                if (flags[1]) {
-                    __threadfence();
-                    const float* tile_part = a.partials + (size_t)m_tile * a.splits * a.n_pad * BM;
-                    if (o < h_out) {
-                        for (int t = 0; t < n; ++t) {
-                            float v = 0.f;
-                            for (int sp = 0; sp < a.splits; ++sp)
-                                v += __ldcg(tile_part + ((size_t)sp * a.n_pad + t) * BM + row);
-                            if (a.fuse) {
-                                const int s = __ldcg(a.seg.idx + t);
-                                if (s >= 0)
-                                    v += lora_term<T>(B + ((size_t)s * h_out + o) * R, a.s_in + (size_t)t * R, R);
-                            }
-                            y[(size_t)t * h_out + o] = from_f32<T>(v);
-                        }
-                    }
-                    if (threadIdx.x == 64) a.counters[m_tile] = 0;  // leave the counter at rest
-                }
             }
         }
     }
+
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // every CTA of the cluster has parked its partial tile
+
+    // ---- epilogue part 2: reduce this CTA's tokens over the cluster, add LoRA, store ----
+    if (warp >= 2 && flags[1]) {
+        const uint32_t p_addr = smem_u32(P) + static_cast<uint32_t>((t0 * BM + row) * 4);
+        for (int q0 = 0; q0 < cnt; q0 += 8) {  // 8 tokens x up to 8 cluster ranks of loads in flight
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                if (c < a.splits) {
+                    const uint32_t base_c = mapa_shared(p_addr, c);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (q0 + u < cnt) v[u] += ld_dsmem_f32(base_c + static_cast<uint32_t>((q0 + u) * BM * 4));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (q0 + u < cnt) Y_sm[(q0 + u) * BM + row] = v[u];
+        }
+        if (a.fuse) {
+            const int D = flags[2];
+            const T* B = static_cast<const T*>(a.pool.B);
+            const int chunks = R / 8;  // 16-byte chunks per B row
+            for (int g0 = 0; g0 < D; g0 += dcap) {
+                const int Dg = min(dcap, D - g0);
+                named_bar_sync(1, 128);
+                for (int e = et; e < Dg * BM * chunks; e += 128) {
+                    const int d = e / (BM * chunks);
+                    const int rem = e % (BM * chunks);
+                    const int rr = rem / chunks, jc = rem % chunks;
+                    const int oo = m_tile * BM + rr;
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (oo < h_out) v = __ldg(reinterpret_cast<const uint4*>(B + ((size_t)dlist[g0 + d] * h_out + oo) * R + jc * 8));
+                    reinterpret_cast<uint4*>(B_sm)[(size_t)(d * BM + rr) * chunks + jc] = v;
+                }
+                named_bar_sync(1, 128);
+                for (int q = 0; q < cnt; ++q) {
+                    const int d = dloc_sm[q] - g0;
+                    if (d < 0 || d >= Dg) continue;
+                    const uint4* br = reinterpret_cast<const uint4*>(B_sm) + (size_t)(d * BM + row) * chunks;
+                    const float* sr = S_sm + q * R;
+                    float acc = 0.f;
+                    for (int jc = 0; jc < chunks; ++jc) {
+                        float b[8];
+                        unpack8<T>(br[jc], b);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc = fmaf(b[e], sr[jc * 8 + e], acc);
+                    }
+                    Y_sm[q * BM + row] += acc;
+                }
+            }
+        }
+        if (o < h_out) {
+            T* y = static_cast<T*>(a.y);
+            for (int q = 0; q < cnt; ++q) y[(size_t)(t0 + q) * h_out + o] = from_f32<T>(Y_sm[q * BM + row]);
+        }
+    }
+    cluster_sync();  // nobody leaves while its partial tile may still be read
     if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
 
@@ -354,7 +427,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     tma_load_2d(smem + d * stage_bytes, &tmX, &full[d], def_kb[d] * BK, def_m[d]);
             }
             if (flags[0]) {
-                report_timeout(a.seg.status);
+                report_timeout_status(a.seg.status);
                 for (int i = max(0, it - stages); i < it; ++i) {
                     const unsigned long long t0 = globaltimer();
                     while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
@@ -392,7 +465,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 }
                 umma_commit(&acc_full[buf]);
             }
-            if (!ok) report_timeout(a.seg.status);
+            if (!ok) report_timeout_status(a.seg.status);
         }
     } else {
         // ---- epilogue: thread <-> token row (TMEM lane), 256 features per tile ----
@@ -431,7 +504,30 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 if (slot >= 0) {
                     const T* Bt = B + ((size_t)slot * h_out + n0 + c0) * R;
                     const int cmax = min(16, h_out - (n0 + c0));
-                    for (int c = 0; c < cmax; ++c) v[c] += lora_term<T>(Bt + (size_t)c * R, srow, R);
+                    for (int j0 = 0; j0 < R; j0 += 8) {
+                        const float4 sa = __ldg(reinterpret_cast<const float4*>(srow + j0));
+                        const float4 sb = __ldg(reinterpret_cast<const float4*>(srow + j0 + 4));
+                        uint4 bv[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            bv[c] = c < cmax ? __ldg(reinterpret_cast<const uint4*>(Bt + (size_t)c * R + j0))
+                                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            float b[8];
+                            unpack8<T>(bv[c], b);
+                            float acc = v[c];
+                            acc = fmaf(b[0], sa.x, acc);
+                            acc = fmaf(b[1], sa.y, acc);
+                            acc = fmaf(b[2], sa.z, acc);
+                            acc = fmaf(b[3], sa.w, acc);
+                            acc = fmaf(b[4], sb.x, acc);
+                            acc = fmaf(b[5], sb.y, acc);
+                            acc = fmaf(b[6], sb.z, acc);
+                            acc = fmaf(b[7], sb.w, acc);
+                            v[c] = acc;
+                        }
+                    }
                 }
                 T* yp = y + (size_t)t * h_out + n0 + c0;
                 alignas(16) T outv[16];
@@ -457,40 +553,17 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 // host side
 // ============================================================================================
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// Row-major [rows, cols] 16-bit matrix, box {64 columns, box_rows rows}, 128-byte swizzle,
-// out-of-bounds elements read as zero.
-static int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t cols, uint64_t rows, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return LORA_OK;
-}
-
 struct DecodePlan {
     int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols;
     size_t smem;
 };
+
+// Epilogue scratch carved from the (then idle) pipeline stages; see gemm_decode_kernel.
+static size_t decode_epilogue_bytes(int n_pad, int splits, int R, size_t elem) {
+    const int per = (n_pad + splits - 1) / splits;
+    size_t b = (size_t)n_pad * BM * 4 + (size_t)per * 4 * 4 + (size_t)per * R * 4 + (size_t)per * BM * 4 + 16;
+    return b + (size_t)BM * R * elem;  // room for at least one adapter's B tile
+}
 
 static DecodePlan plan_decode(const PoolView& pv, int n) {
     DecodePlan p;
@@ -499,12 +572,15 @@ static DecodePlan plan_decode(const PoolView& pv, int n) {
     p.kb_total = (pv.h_in + BK - 1) / BK;
     const int sms = num_sms();
     int splits = std::max(1, sms / p.m_tiles);
+    splits = std::min(splits, 8);  // portable cluster size
     splits = std::min(splits, std::max(1, p.kb_total / 4));
     p.kb_per_split = (p.kb_total + splits - 1) / splits;
     p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
     const int stage_bytes = BM * BK * 2 + p.n_pad * BK * 2;
     p.stages = std::max(2, std::min(8, kSmemBudget / stage_bytes));
-    p.stages = std::min(p.stages, std::max(2, p.kb_per_split));
+    // the epilogue reuses the stage area: make it large enough
+    const size_t need = decode_epilogue_bytes(p.n_pad, p.splits, pv.R, 2);
+    while ((size_t)p.stages * stage_bytes < need) ++p.stages;
     int cols = 32;
     while (cols < p.n_pad) cols <<= 1;
     p.tmem_cols = cols;
@@ -517,32 +593,19 @@ static DecodePlan plan_decode(const PoolView& pv, int n) {
 int tc_supported(const PoolView& pv, int n) {
     if (pv.dtype != LORA_F16 && pv.dtype != LORA_BF16) return 0;
     if (pv.h_in % 8 || pv.h_out % 8 || pv.R % 8) return 0;
-    (void)n;
+    if (n > 0 && n <= tc::kDecodeMaxN && tc::plan_decode(pv, n).smem > (size_t)(227 * 1024)) return 0;
     return 1;
-}
-
-size_t tc_workspace_floats(const PoolView& pv, int n, int* counters) {
-    if (n <= 0 || n > tc::kDecodeMaxN || !tc_supported(pv, n)) {
-        *counters = 0;
-        return 0;
-    }
-    const tc::DecodePlan p = tc::plan_decode(pv, n);
-    *counters = p.m_tiles;
-    return p.splits > 1 ? (size_t)p.m_tiles * p.splits * p.n_pad * tc::BM : 0;
 }
 
 template <typename T>
 static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                       bool fuse, const TcWorkspace& ws, cudaStream_t st) {
+                       bool fuse, cudaStream_t st) {
     using namespace tc;
     const int n = sv.n;
     if (n == 0) return LORA_OK;
     const int bf16 = pv.dtype == LORA_BF16;
     if (n <= kDecodeMaxN) {
         const DecodePlan p = plan_decode(pv, n);
-        if (p.splits > 1 && (!ws.partials || !ws.counters || ws.partial_floats < (size_t)p.m_tiles * p.splits * p.n_pad * BM ||
-                             ws.counter_count < p.m_tiles))
-            return set_error(LORA_ENOSPACE, "decode split-K workspace too small");
         CUtensorMap mW, mX;
         int rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, BM);
         if (rc) return rc;
@@ -553,8 +616,6 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.seg = sv;
         a.s_in = s_in;
         a.y = y;
-        a.partials = ws.partials;
-        a.counters = ws.counters;
         a.n = n;
         a.n_pad = p.n_pad;
         a.kb_total = p.kb_total;
@@ -564,15 +625,30 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.tmem_cols = p.tmem_cols;
         a.fuse = fuse ? 1 : 0;
         a.bf16 = bf16;
-        static bool attr = false;
-        if (!attr) {
+        static bool attr_set = false;
+        if (!attr_set) {
             LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmemBudget + 8 * 1024));
-            attr = true;
+                                               227 * 1024));
+            attr_set = true;
         }
         void* args[] = {(void*)&mW, (void*)&mX, (void*)&a};
-        LORA_CUDA_TRY(launch_pdl((const void*)gemm_decode_kernel<T>, dim3(p.m_tiles, p.splits), dim3(kThreads), p.smem,
-                                 st, args));
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(p.m_tiles, p.splits);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = p.smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = p.splits;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        LORA_CUDA_TRY(cudaLaunchKernelExC(&cfg, (const void*)gemm_decode_kernel<T>, args));
+        count_launch();
         return LORA_OK;
     }
     // prefill
@@ -609,9 +685,9 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
 }
 
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                   bool fuse, const TcWorkspace& ws, cudaStream_t st) {
-    if (pv.dtype == LORA_F16) return launch_tc_t<__half>(pv, sv, W, x, s_in, y, fuse, ws, st);
-    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, y, fuse, ws, st);
+                   bool fuse, cudaStream_t st) {
+    if (pv.dtype == LORA_F16) return launch_tc_t<__half>(pv, sv, W, x, s_in, y, fuse, st);
+    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, y, fuse, st);
 }
 
 }  // namespace lora

@@ -17,19 +17,16 @@ int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const
                      bool fuse, cudaStream_t st);
 
 // Tensor-core (tcgen05) base GEMM with optional fused expand.
-//   decode path  (n <= 256): W tiles on the MMA M side, tokens on N, split-K with an
-//                 in-kernel last-CTA reduction (partials + counters in ws).
+//   decode path  (n <= 256): W tiles on the MMA M side, tokens on N, split-K across the CTAs
+//                 of a thread-block cluster, reduced through distributed shared memory.
 //   prefill path (n > 256):  token tiles on M (128), outputs on N (256), persistent CTAs.
-struct TcWorkspace {
-    float* partials;     // decode split-K partials
-    int32_t* counters;   // decode split-K arrival counters (zero at rest)
-    size_t partial_floats;
-    int counter_count;
-};
 int tc_supported(const PoolView& pv, int n);
-size_t tc_workspace_floats(const PoolView& pv, int n, int* counters);
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                   bool fuse, const TcWorkspace& ws, cudaStream_t st);
+                   bool fuse, cudaStream_t st);
+
+// Grouped tcgen05 shrink for batches of more than 256 tokens (one CTA per 128-token tile).
+int shrink_tc_supported(const PoolView& pv);
+int launch_shrink_tc(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st);
 
 int num_sms();
 

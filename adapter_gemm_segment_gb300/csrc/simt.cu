@@ -70,6 +70,65 @@ shrink_warp_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* _
     }
 }
 
+// ---- shrink for small batches: one CTA per (sorted token, 8 adapter rows) ---------------------
+// 256 threads each own 8 consecutive input features of every 2048-feature sweep; a 4096-wide
+// row is two sweeps, unrolled so that all 18 16-byte loads of a thread are in flight together.
+template <typename T>
+__global__ void __launch_bounds__(256)
+shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
+    __shared__ float red[8][8];
+    pdl_wait();
+    pdl_trigger();
+    if (*seg.status != LORA_OK) return;
+    const int j = blockIdx.x, g = blockIdx.y;
+    if (j >= seg.n) return;
+    const int t = seg.perm[j];
+    const int s = seg.idx[t];
+    if (s < 0) return;
+    const int h = pool.h_in, R = pool.R;
+    const T* xr = x + (size_t)t * h;
+    const T* Ar = static_cast<const T*>(pool.A) + ((size_t)s * R + (size_t)g * 8) * h;
+    float acc[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) acc[r] = 0.f;
+    for (int k0 = threadIdx.x * 8; k0 < h; k0 += 2 * 2048) {
+        const int k1 = k0 + 2048;
+        const bool two = k1 < h;
+        uint4 xv0 = *reinterpret_cast<const uint4*>(xr + k0);
+        uint4 xv1 = two ? *reinterpret_cast<const uint4*>(xr + k1) : make_uint4(0, 0, 0, 0);
+        uint4 av0[8], av1[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            av0[r] = __ldg(reinterpret_cast<const uint4*>(Ar + (size_t)r * h + k0));
+            av1[r] = two ? __ldg(reinterpret_cast<const uint4*>(Ar + (size_t)r * h + k1)) : make_uint4(0, 0, 0, 0);
+        }
+        float xf0[8], xf1[8];
+        unpack8<T>(xv0, xf0);
+        unpack8<T>(xv1, xf1);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            float a0[8], a1[8];
+            unpack8<T>(av0[r], a0);
+            unpack8<T>(av1[r], a1);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[r] = fmaf(xf0[e], a0[e], fmaf(xf1[e], a1[e], acc[r]));
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const float v = warp_sum(acc[r]);
+        if (lane == 0) red[warp][r] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 8) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v += red[w][threadIdx.x];
+        s_out[(size_t)t * R + g * 8 + threadIdx.x] = pool.table[s].scale * v;
+    }
+}
+
 // ---- shrink, tiled: one CTA per (segment, 64 sorted tokens) -----------------------------------
 // For long segments (prefill) x and A are staged through shared memory in K-chunks of 64 and
 // every thread keeps a 4 x (R/16) register tile.
@@ -287,6 +346,15 @@ template <typename T>
 static int launch_shrink_t(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st,
                            bool tiled) {
     const T* xp = static_cast<const T*>(x);
+    if constexpr (sizeof(T) == 2) {
+        if (!tiled) {
+            if (sv.n == 0) return LORA_OK;
+            void* args[] = {(void*)&pv, (void*)&sv, (void*)&xp, (void*)&s_out};
+            LORA_CUDA_TRY(
+                launch_pdl((const void*)shrink_token_kernel<T>, dim3(sv.n, pv.R / 8), dim3(256), 0, st, args));
+            return LORA_OK;
+        }
+    }
     if (!tiled) {
         const int RG = (pv.R % 8 == 0) ? 8 : 1;
         const long warps = (long)sv.n * (pv.R / RG);

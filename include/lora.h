@@ -165,8 +165,8 @@ int lora_linear_workspace_bytes(lora_pool_t pool, int n_tokens, size_t* bytes);
  *   W_dev [h_out, h_in], x_dev [n, h_in], y_dev [n, h_out]: device, pool dtype, 16-byte
  *   aligned for 16-bit dtypes; n = seg->n_tokens; seg from lora_segment on this pool's
  *   slot count; variant a lora_variant; ws_dev device workspace of
- *   >= lora_linear_workspace_bytes, 256-byte aligned, zero-filled before its first use
- *   (every call leaves its counter region zeroed again).
+ *   >= lora_linear_workspace_bytes, 256-byte aligned (it receives the shrink output
+ *   s = (alpha/r) x A^T, float32 [n, r_max]; successive calls on one stream may share it).
  * If seg's status word is not LORA_OK the kernels leave y untouched. */
 int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
                     const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes, void* stream);
