@@ -304,14 +304,31 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int g0 = 0; g0 < D; g0 += dcap) {
                 const int Dg = min(dcap, D - g0);
                 named_bar_sync(1, 128);
-                for (int e = et; e < Dg * BM * chunks; e += 128) {
-                    const int d = e / (BM * chunks);
-                    const int rem = e % (BM * chunks);
-                    const int rr = rem / chunks, jc = rem % chunks;
-                    const int oo = m_tile * BM + rr;
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (oo < h_out) v = __ldg(reinterpret_cast<const uint4*>(B + ((size_t)dlist[g0 + d] * h_out + oo) * R + jc * 8));
-                    reinterpret_cast<uint4*>(B_sm)[(size_t)(d * BM + rr) * chunks + jc] = v;
+                // stage B rows of the group's slots: 8 independent 16-byte loads in flight per thread
+                const int total = Dg * BM * chunks;
+                for (int e0 = et; e0 < total; e0 += 8 * 128) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = e0 + u * 128;
+                        v[u] = make_uint4(0, 0, 0, 0);
+                        if (e < total) {
+                            const int d = e / (BM * chunks);
+                            const int rem = e - d * (BM * chunks);
+                            const int oo = m_tile * BM + rem / chunks;
+                            if (oo < h_out)
+                                v[u] = __ldg(reinterpret_cast<const uint4*>(B + ((size_t)dlist[g0 + d] * h_out + oo) * R +
+                                                                             (rem % chunks) * 8));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = e0 + u * 128;
+                        if (e < total) {
+                            const int d = e / (BM * chunks);
+                            reinterpret_cast<uint4*>(B_sm)[(size_t)d * BM * chunks + (e - d * (BM * chunks))] = v[u];
+                        }
+                    }
                 }
                 named_bar_sync(1, 128);
                 for (int q = 0; q < cnt; ++q) {
