@@ -74,7 +74,8 @@ static void record_if(cudaEvent_t e, cudaStream_t st) {
 constexpr int kFusedMinTokens = 1;
 constexpr int kVariantCudaCore = LORA_VARIANT_CUDA_CORE;
 
-// Linear workspace: the shrink output s [n, r_max] float32 (alpha/r folded in).
+// Linear workspace: the shrink output, up to ceil(h_in/1024) K-parts of float32 [n, r_max]
+// (alpha/r folded in).
 struct LinWsLayout {
     size_t s_off, total;
 };
@@ -82,7 +83,8 @@ struct LinWsLayout {
 static LinWsLayout lin_layout(const PoolView& pv, int n) {
     LinWsLayout L;
     L.s_off = 0;
-    L.total = align256(sizeof(float) * (size_t)(n > 0 ? n : 1) * pv.R);
+    const int parts = shrink_parts(pv, n, false);
+    L.total = align256(sizeof(float) * (size_t)(n > 0 ? n : 1) * pv.R * (size_t)parts);
     return L;
 }
 
@@ -147,21 +149,22 @@ int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void
     const bool fused = variant != LORA_VARIANT_SEPARATE;
     record_if(g_ev_before_shrink, st);
     int rc;
+    int s_parts = 1;
     if (tc && n > 256 && shrink_tc_supported(pv))
         rc = launch_shrink_tc(pv, sv, x_dev, s_buf, st);
     else
-        rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256);
+        rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256, &s_parts);
     if (rc) return rc;
     record_if(g_ev_before_gemm, st);
     if (tc) {
-        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, st);
+        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
     } else {
-        rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, y_dev, fused, st);
+        rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
     }
     if (rc) return rc;
     record_if(g_ev_after_gemm, st);
     if (!fused) {
-        rc = launch_expand(pv, sv, s_buf, y_dev, st);
+        rc = launch_expand(pv, sv, s_buf, s_parts, y_dev, st);
         if (rc) return rc;
     }
     return LORA_OK;

@@ -50,6 +50,8 @@ struct DecodeArgs {
     const float* s_in;
     void* y;
     int n, n_pad, kb_total, splits, kb_per_split, stages, tmem_cols, fuse, bf16;
+    int s_parts;  // K-parts of the shrink output to sum
+    int dpre;     // distinct slots whose B rows are staged during the main loop
 };
 
 struct PrefillArgs {
@@ -85,10 +87,13 @@ __device__ __forceinline__ float lora_term(const T* __restrict__ Brow, const flo
 // decode: swap-AB + split-K over a thread-block cluster
 // ============================================================================================
 // The `splits` CTAs that share one 128-feature tile form a cluster (cluster dims 1 x splits).
-// After its K range, every CTA parks its float32 partial tile [n_pad tokens][128 features] in
-// its own shared memory (the pipeline stages are free by then); after a cluster barrier CTA r
-// sums the partials of tokens [r*per, (r+1)*per) over the cluster through distributed shared
-// memory, adds the LoRA term of those tokens and writes y.  No global scratch, no atomics.
+// While the MMA warp streams W, the epilogue warps already stage everything the LoRA term needs
+// for this CTA's share of tokens (slot ids, the distinct slots, s summed over its K-parts, and
+// the B rows of those slots) into a dedicated shared-memory region.  After its K range every
+// CTA parks its float32 partial tile [n_pad tokens][128 features] in the (then idle) pipeline
+// stages; after a cluster barrier CTA r sums the partials of tokens [r*per, (r+1)*per) over the
+// cluster through distributed shared memory, adds the LoRA term and writes y.  No global
+// scratch, no atomics.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -99,11 +104,21 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const uint32_t w_bytes = BM * BK * 2;
     const uint32_t x_bytes = static_cast<uint32_t>(a.n_pad) * BK * 2;
     const uint32_t stage_bytes = w_bytes + x_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
+    const int R = a.pool.R;
+    const int per = (a.n_pad + a.splits - 1) / a.splits;  // tokens reduced by each CTA
+    // dedicated LoRA staging region after the stages
+    int* slot_sm = reinterpret_cast<int*>(smem + (size_t)stages * stage_bytes);  // [per]
+    int* dloc_sm = slot_sm + per;                                               // [per]
+    int* dlist = dloc_sm + per;                                                 // [per]
+    int* fidx_sm = dlist + per;                                                 // [per]
+    float* S_sm = reinterpret_cast<float*>(fidx_sm + per);                      // [per][R]
+    T* Bpre = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(S_sm + (size_t)per * R + 3) & ~uintptr_t(15));
+    uint64_t* full = reinterpret_cast<uint64_t*>(
+        (reinterpret_cast<uintptr_t>(Bpre + (size_t)a.dpre * BM * R) + 7) & ~uintptr_t(7));
     uint64_t* empty = full + stages;
     uint64_t* tmem_full = empty + stages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
-    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort, go, distinct count
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort, go, D, status, wsum[4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, split = blockIdx.y;
@@ -116,9 +131,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             mbar_init(&empty[s], 1);
         }
         mbar_init(tmem_full, 1);
-        flags[0] = 0;
-        flags[1] = 0;
-        flags[2] = 0;
+        for (int i = 0; i < 8; ++i) flags[i] = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -135,23 +148,25 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const uint32_t tmem = *tmem_slot;
     pdl_trigger();
 
+    const int et = threadIdx.x - 64;  // 0..127 in the epilogue warps
+    const int row = (warp & 3) * 32 + lane;
+    const int o = m_tile * BM + row;
+    const int h_out = a.pool.h_out, n = a.n;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int t0 = rank * per;
+    const int cnt = max(0, min(n, t0 + per) - t0);
+    const int chunks = R / 8;  // 16-byte chunks per B row
+    const T* B = static_cast<const T*>(a.pool.B);
+
     if (warp == 0) {
         if (lane == 0) {
-            // W does not depend on earlier kernels: fill the whole ring with W tiles first, then
-            // wait for the previous grid before reading x.
-            const int pre = min(stages, nkb);
-            for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], stage_bytes);
-                tma_load_2d(smem + i * stage_bytes, &tmW, &full[i], (kb0 + i) * BK, m_tile * BM);
-            }
-            pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem + i * stage_bytes + w_bytes, &tmX, &full[i], (kb0 + i) * BK, 0);
-            int issued = pre;
-            for (int i = pre; i < nkb; ++i) {
+            // x is complete before this grid starts: the preceding shrink kernel releases its
+            // dependents only after its own grid-dependency wait.
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
                 const int s = i % stages;
                 const uint32_t ph = (i / stages) & 1;
-                if (!mbar_wait(&empty[s], ph ^ 1, flags)) break;
+                if (i >= stages && !mbar_wait(&empty[s], ph ^ 1, flags)) break;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tma_load_2d(smem + s * stage_bytes, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM);
                 tma_load_2d(smem + s * stage_bytes + w_bytes, &tmX, &full[s], (kb0 + i) * BK, 0);
@@ -160,8 +175,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (flags[0]) {  // aborted: let copies already in flight land before the CTA exits
                 report_timeout_status(a.seg.status);
                 for (int i = max(0, issued - stages); i < issued; ++i) {
-                    const unsigned long long t0 = globaltimer();
-                    while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+                    const unsigned long long tw = globaltimer();
+                    while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - tw < kWaitLimitNs) {
                     }
                 }
             }
@@ -186,36 +201,90 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
             umma_commit(tmem_full);  // also on abort: fires once the issued MMAs have finished
         }
-    }
-
-    // ---- epilogue part 1 (warps 2..5): park the partial tile, stage this CTA's LoRA operands ----
-    const int et = threadIdx.x - 64;  // 0..127 in the epilogue warps
-    const int row = (warp & 3) * 32 + lane;
-    const int o = m_tile * BM + row;
-    const int h_out = a.pool.h_out, R = a.pool.R, n = a.n;
-    const int per = (a.n_pad + a.splits - 1) / a.splits;  // tokens reduced by each CTA
-    const int rank = static_cast<int>(cluster_ctarank());
-    const int t0 = rank * per;
-    const int cnt = max(0, min(n, t0 + per) - t0);
-    float* P = reinterpret_cast<float*>(smem);                       // [n_pad][128]
-    int* slot_sm = reinterpret_cast<int*>(P + (size_t)a.n_pad * BM);  // [per]
-    int* dloc_sm = slot_sm + per;                                     // [per]
-    int* dlist = dloc_sm + per;                                       // [per]
-    int* fidx_sm = dlist + per;                                       // [per]
-    float* S_sm = reinterpret_cast<float*>(fidx_sm + per);            // [per][R]
-    float* Y_sm = S_sm + (size_t)per * R;                             // [per][128]
-    T* B_sm = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(Y_sm + (size_t)per * BM + 3) & ~uintptr_t(15));
-    const size_t b_cap_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(B_sm) - smem);
-    const int dcap = static_cast<int>(b_cap_bytes / ((size_t)BM * R * sizeof(T)));
-    if (warp >= 2) {
+    } else {
+        // ---- epilogue phase A (overlaps the main loop): stage this CTA's LoRA operands ----
+        pdl_wait();  // s, idx and the status word come from earlier kernels
+        if (et == 0) flags[3] = __ldcg(a.seg.status);
+        named_bar_sync(1, 128);
+        if (flags[3] == LORA_OK && a.fuse) {
+            for (int q = et; q < cnt; q += 128) slot_sm[q] = __ldcg(a.seg.idx + t0 + q);
+            named_bar_sync(1, 128);
+            // distinct slots of this CTA's tokens: dloc_sm[q] = index of token q's slot in dlist
+            for (int q = et; q < cnt; q += 128) {
+                int first = -1;
+                if (slot_sm[q] >= 0) {
+                    first = q;
+                    for (int q2 = 0; q2 < q; ++q2)
+                        if (slot_sm[q2] == slot_sm[q]) {
+                            first = q2;
+                            break;
+                        }
+                }
+                fidx_sm[q] = first;
+            }
+            int* wsum = const_cast<int*>(flags) + 4;
+            int running = 0;
+            for (int c0 = 0; c0 < cnt; c0 += 128) {  // block-wide exclusive scan of "first occurrence"
+                const int q = c0 + et;
+                named_bar_sync(1, 128);
+                const bool is_first = q < cnt && fidx_sm[q] == q;
+                const unsigned bal = __ballot_sync(0xffffffffu, is_first);
+                if (lane == 0) wsum[et >> 5] = __popc(bal);
+                named_bar_sync(1, 128);
+                int base = running;
+                for (int w = 0; w < (et >> 5); ++w) base += wsum[w];
+                if (is_first) {
+                    const int d = base + __popc(bal & ((1u << lane) - 1u));
+                    dloc_sm[q] = d;
+                    dlist[d] = slot_sm[q];
+                }
+                running += wsum[0] + wsum[1] + wsum[2] + wsum[3];
+            }
+            if (et == 0) flags[2] = running;
+            named_bar_sync(1, 128);
+            for (int q = et; q < cnt; q += 128) {
+                const int f = fidx_sm[q];
+                if (f != q) dloc_sm[q] = f >= 0 ? dloc_sm[f] : -1;
+            }
+            // s of this CTA's tokens, summed over the shrink's K-parts
+            for (int e = et; e < cnt * R; e += 128) {
+                const int q = e / R, j = e - q * R;
+                float v = 0.f;
+                if (slot_sm[q] >= 0)
+                    for (int k = 0; k < a.s_parts; ++k) v += __ldcg(a.s_in + ((size_t)k * n + t0 + q) * R + j);
+                S_sm[e] = v;
+            }
+            // B rows of the first dpre distinct slots
+            const int Dg = min(running, a.dpre);
+            const int total = Dg * BM * chunks;
+            for (int e0 = et; e0 < total; e0 += 8 * 128) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = e0 + u * 128;
+                    v[u] = make_uint4(0, 0, 0, 0);
+                    if (e < total) {
+                        const int d = e / (BM * chunks);
+                        const int rem = e - d * (BM * chunks);
+                        const int oo = m_tile * BM + rem / chunks;
+                        if (oo < h_out)
+                            v[u] = __ldg(reinterpret_cast<const uint4*>(B + ((size_t)dlist[d] * h_out + oo) * R +
+                                                                         (rem % chunks) * 8));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (e0 + u * 128 < total) reinterpret_cast<uint4*>(Bpre)[e0 + u * 128] = v[u];
+            }
+        }
+        // ---- epilogue phase B: park the partial tile in the idle pipeline stages ----
         const bool got = mbar_wait(tmem_full, 0, flags);
         tc_fence_after();
-        pdl_wait();
-        const int status = __ldcg(a.seg.status);
         named_bar_sync(1, 128);
-        if (et == 0) flags[1] = (got && !flags[0] && status == LORA_OK && dcap >= 1) ? 1 : 0;
+        if (et == 0) flags[1] = (got && !flags[0] && flags[3] == LORA_OK) ? 1 : 0;
         named_bar_sync(1, 128);
         if (flags[1]) {
+            float* P = reinterpret_cast<float*>(smem);  // [n_pad][128]
             const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             for (int c0 = 0; c0 < a.n_pad; c0 += 16) {
                 uint32_t r[16];
@@ -225,60 +294,16 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 #pragma unroll
                 for (int c = 0; c < 16; ++c) P[(c0 + c) * BM + row] = __uint_as_float(r[c]);
             }
-            if (a.fuse) {
-                for (int q = et; q < cnt; q += 128) slot_sm[q] = __ldcg(a.seg.idx + t0 + q);
-                named_bar_sync(1, 128);
-                // distinct slots of this CTA's tokens: dloc_sm[q] = index of token q's slot in dlist
-                for (int q = et; q < cnt; q += 128) {
-                    int first = -1;
-                    if (slot_sm[q] >= 0) {
-                        first = q;
-                        for (int q2 = 0; q2 < q; ++q2)
-                            if (slot_sm[q2] == slot_sm[q]) {
-                                first = q2;
-                                break;
-                            }
-                    }
-                    fidx_sm[q] = first;
-                }
-                int* wsum = reinterpret_cast<int*>(const_cast<int*>(flags)) + 4;  // 4 ints
-                int running = 0;
-                for (int c0 = 0; c0 < cnt; c0 += 128) {  // block-wide exclusive scan of "first occurrence"
-                    const int q = c0 + et;
-                    named_bar_sync(1, 128);
-                    const bool is_first = q < cnt && fidx_sm[q] == q;
-                    const unsigned bal = __ballot_sync(0xffffffffu, is_first);
-                    if (lane == 0) wsum[(et >> 5)] = __popc(bal);
-                    named_bar_sync(1, 128);
-                    int base = running;
-                    for (int w = 0; w < (et >> 5); ++w) base += wsum[w];
-                    if (is_first) {
-                        const int d = base + __popc(bal & ((1u << lane) - 1u));
-                        dloc_sm[q] = d;
-                        dlist[d] = slot_sm[q];
-                    }
-                    running += wsum[0] + wsum[1] + wsum[2] + wsum[3];
-                }
-                if (et == 0) flags[2] = running;
-                named_bar_sync(1, 128);
-                for (int q = et; q < cnt; q += 128) {
-                    const int f = fidx_sm[q];
-                    if (f != q) dloc_sm[q] = f >= 0 ? dloc_sm[f] : -1;
-                }
-                for (int e = et; e < cnt * R; e += 128) {
-                    const int q = e / R;
-                    S_sm[e] = slot_sm[q] >= 0 ? __ldcg(a.s_in + (size_t)(t0 + q) * R + (e % R)) : 0.f;
-                }
-                named_bar_sync(1, 128);
-            }
         }
     }
 
     tc_fence_before();
     cluster_sync();  // every CTA of the cluster has parked its partial tile
 
-    // ---- epilogue part 2: reduce this CTA's tokens over the cluster, add LoRA, store ----
+    // ---- epilogue phase C: reduce this CTA's tokens over the cluster, add LoRA, store ----
     if (warp >= 2 && flags[1]) {
+        float* P = reinterpret_cast<float*>(smem);
+        float* Y_sm = P + (size_t)a.n_pad * BM;  // [per][128]
         const uint32_t p_addr = smem_u32(P) + static_cast<uint32_t>((t0 * BM + row) * 4);
         for (int q0 = 0; q0 < cnt; q0 += 8) {  // 8 tokens x up to 8 cluster ranks of loads in flight
             float v[8];
@@ -299,42 +324,42 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         if (a.fuse) {
             const int D = flags[2];
-            const T* B = static_cast<const T*>(a.pool.B);
-            const int chunks = R / 8;  // 16-byte chunks per B row
-            for (int g0 = 0; g0 < D; g0 += dcap) {
-                const int Dg = min(dcap, D - g0);
-                named_bar_sync(1, 128);
-                // stage B rows of the group's slots: 8 independent 16-byte loads in flight per thread
-                const int total = Dg * BM * chunks;
-                for (int e0 = et; e0 < total; e0 += 8 * 128) {
-                    uint4 v[8];
+            // slots beyond the pre-staged ones are staged now, after Y_sm, in groups
+            T* Blate = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(Y_sm + (size_t)per * BM + 3) & ~uintptr_t(15));
+            const size_t late_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(Blate) - smem);
+            const int dlate = max(1, static_cast<int>(late_bytes / ((size_t)BM * R * sizeof(T))));
+            for (int g0 = 0; g0 < D;) {
+                const bool pre = g0 == 0 && a.dpre > 0;
+                const int Dg = pre ? min(D, a.dpre) : min(D - g0, dlate);
+                const T* Bg = pre ? Bpre : Blate;
+                if (!pre) {
+                    named_bar_sync(1, 128);
+                    const int total = Dg * BM * chunks;
+                    for (int e0 = et; e0 < total; e0 += 8 * 128) {
+                        uint4 v[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int e = e0 + u * 128;
-                        v[u] = make_uint4(0, 0, 0, 0);
-                        if (e < total) {
-                            const int d = e / (BM * chunks);
-                            const int rem = e - d * (BM * chunks);
-                            const int oo = m_tile * BM + rem / chunks;
-                            if (oo < h_out)
-                                v[u] = __ldg(reinterpret_cast<const uint4*>(B + ((size_t)dlist[g0 + d] * h_out + oo) * R +
-                                                                             (rem % chunks) * 8));
+                        for (int u = 0; u < 8; ++u) {
+                            const int e = e0 + u * 128;
+                            v[u] = make_uint4(0, 0, 0, 0);
+                            if (e < total) {
+                                const int d = e / (BM * chunks);
+                                const int rem = e - d * (BM * chunks);
+                                const int oo = m_tile * BM + rem / chunks;
+                                if (oo < h_out)
+                                    v[u] = __ldg(reinterpret_cast<const uint4*>(
+                                        B + ((size_t)dlist[g0 + d] * h_out + oo) * R + (rem % chunks) * 8));
+                            }
                         }
-                    }
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int e = e0 + u * 128;
-                        if (e < total) {
-                            const int d = e / (BM * chunks);
-                            reinterpret_cast<uint4*>(B_sm)[(size_t)d * BM * chunks + (e - d * (BM * chunks))] = v[u];
-                        }
+                        for (int u = 0; u < 8; ++u)
+                            if (e0 + u * 128 < total) reinterpret_cast<uint4*>(Blate)[e0 + u * 128] = v[u];
                     }
+                    named_bar_sync(1, 128);
                 }
-                named_bar_sync(1, 128);
                 for (int q = 0; q < cnt; ++q) {
                     const int d = dloc_sm[q] - g0;
                     if (d < 0 || d >= Dg) continue;
-                    const uint4* br = reinterpret_cast<const uint4*>(B_sm) + (size_t)(d * BM + row) * chunks;
+                    const uint4* br = reinterpret_cast<const uint4*>(Bg) + (size_t)(d * BM + row) * chunks;
                     const float* sr = S_sm + q * R;
                     float acc = 0.f;
                     for (int jc = 0; jc < chunks; ++jc) {
@@ -345,6 +370,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     }
                     Y_sm[q * BM + row] += acc;
                 }
+                g0 += Dg;
             }
         }
         if (o < h_out) {
@@ -571,16 +597,9 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 // ============================================================================================
 
 struct DecodePlan {
-    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols;
+    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre;
     size_t smem;
 };
-
-// Epilogue scratch carved from the (then idle) pipeline stages; see gemm_decode_kernel.
-static size_t decode_epilogue_bytes(int n_pad, int splits, int R, size_t elem) {
-    const int per = (n_pad + splits - 1) / splits;
-    size_t b = (size_t)n_pad * BM * 4 + (size_t)per * 4 * 4 + (size_t)per * R * 4 + (size_t)per * BM * 4 + 16;
-    return b + (size_t)BM * R * elem;  // room for at least one adapter's B tile
-}
 
 static DecodePlan plan_decode(const PoolView& pv, int n) {
     DecodePlan p;
@@ -593,15 +612,30 @@ static DecodePlan plan_decode(const PoolView& pv, int n) {
     splits = std::min(splits, std::max(1, p.kb_total / 4));
     p.kb_per_split = (p.kb_total + splits - 1) / splits;
     p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
-    const int stage_bytes = BM * BK * 2 + p.n_pad * BK * 2;
-    p.stages = std::max(2, std::min(8, kSmemBudget / stage_bytes));
-    // the epilogue reuses the stage area: make it large enough
-    const size_t need = decode_epilogue_bytes(p.n_pad, p.splits, pv.R, 2);
-    while ((size_t)p.stages * stage_bytes < need) ++p.stages;
+    const int per = (p.n_pad + p.splits - 1) / p.splits;
+    const size_t stage_bytes = (size_t)BM * BK * 2 + (size_t)p.n_pad * BK * 2;
+    const size_t fixed = (size_t)per * 4 * 4 + (size_t)per * pv.R * 4 + 16 + 2 * 1024 /* barriers, align */;
+    const size_t slot_b = (size_t)BM * pv.R * 2;
+    const int want = std::min(std::min(per, pv.S), 32);
+    const size_t limit = 225 * 1024;
+    p.stages = 4;
+    p.dpre = 0;
+    for (int st = 8; st >= 4; --st) {
+        if ((size_t)st * stage_bytes + fixed > limit) continue;
+        const int dp = (int)std::min<size_t>((size_t)want, (limit - st * stage_bytes - fixed) / slot_b);
+        if (dp >= want || st == 4) {
+            p.stages = st;
+            p.dpre = dp;
+            break;
+        }
+    }
+    // the stage area must also hold the parked partial tile, this CTA's output rows and one late B tile
+    const size_t park = (size_t)p.n_pad * BM * 4 + (size_t)per * BM * 4 + 16 + slot_b;
+    while ((size_t)p.stages * stage_bytes < park) ++p.stages;
     int cols = 32;
     while (cols < p.n_pad) cols <<= 1;
     p.tmem_cols = cols;
-    p.smem = (size_t)p.stages * stage_bytes + 1024 + 256;
+    p.smem = (size_t)p.stages * stage_bytes + fixed + (size_t)p.dpre * slot_b + 1024;
     return p;
 }
 
@@ -615,8 +649,8 @@ int tc_supported(const PoolView& pv, int n) {
 }
 
 template <typename T>
-static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                       bool fuse, cudaStream_t st) {
+static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
+                       int s_parts, void* y, bool fuse, cudaStream_t st) {
     using namespace tc;
     const int n = sv.n;
     if (n == 0) return LORA_OK;
@@ -642,6 +676,8 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.tmem_cols = p.tmem_cols;
         a.fuse = fuse ? 1 : 0;
         a.bf16 = bf16;
+        a.s_parts = s_parts;
+        a.dpre = p.dpre;
         static bool attr_set = false;
         if (!attr_set) {
             LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -669,6 +705,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         return LORA_OK;
     }
     // prefill
+    if (s_parts != 1) return set_error(LORA_EINVAL, "internal: prefill GEMM expects an unsplit shrink output");
     PrefillArgs a;
     a.pool = pv;
     a.seg = sv;
@@ -701,10 +738,10 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     return LORA_OK;
 }
 
-int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                   bool fuse, cudaStream_t st) {
-    if (pv.dtype == LORA_F16) return launch_tc_t<__half>(pv, sv, W, x, s_in, y, fuse, st);
-    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, y, fuse, st);
+int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
+                   void* y, bool fuse, cudaStream_t st) {
+    if (pv.dtype == LORA_F16) return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, st);
+    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, st);
 }
 
 }  // namespace lora

@@ -4,25 +4,31 @@
 
 namespace lora {
 
-// s_out[t, :] = scale_s * x[t] A_s^T for every token with a slot (float32, original order).
-// tiled = one CTA per (segment, 64 tokens) through shared memory; otherwise one warp per
-// (token, 8 adapter rows).
-int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled);
+// Shrink output layout: s_parts float32 arrays [n, r_max] (original token order); the shrink
+// value of token t is scale_s * x[t] A_s^T = sum over parts p of s[p][t][:].  Rows of
+// base-only tokens are not written.
+
+// CUDA-core shrink.  Small batches of 16-bit data: one CTA per (sorted token, 8 adapter rows,
+// 1024 input features), *s_parts = ceil(h_in / 1024).  tiled: one CTA per (segment, 64 tokens)
+// through shared memory, *s_parts = 1.  float32: one warp per (token, rows), *s_parts = 1.
+int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled,
+                  int* s_parts);
+int shrink_parts(const PoolView& pv, int n, bool tiled);
 
 // y[t, :] += s[t, :] B_s^T (separate variant's residual kernel).
-int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, void* y, cudaStream_t st);
+int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, int s_parts, void* y, cudaStream_t st);
 
 // CUDA-core base GEMM y = x W^T (+ fused expand when fuse).
-int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                     bool fuse, cudaStream_t st);
+int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
+                     int s_parts, void* y, bool fuse, cudaStream_t st);
 
 // Tensor-core (tcgen05) base GEMM with optional fused expand.
 //   decode path  (n <= 256): W tiles on the MMA M side, tokens on N, split-K across the CTAs
 //                 of a thread-block cluster, reduced through distributed shared memory.
 //   prefill path (n > 256):  token tiles on M (128), outputs on N (256), persistent CTAs.
 int tc_supported(const PoolView& pv, int n);
-int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                   bool fuse, cudaStream_t st);
+int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
+                   void* y, bool fuse, cudaStream_t st);
 
 // Grouped tcgen05 shrink for batches of more than 256 tokens (one CTA per 128-token tile).
 int shrink_tc_supported(const PoolView& pv);

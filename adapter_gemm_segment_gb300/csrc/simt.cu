@@ -70,48 +70,42 @@ shrink_warp_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* _
     }
 }
 
-// ---- shrink for small batches: one CTA per (sorted token, 8 adapter rows) ---------------------
-// 256 threads each own 8 consecutive input features of every 2048-feature sweep; a 4096-wide
-// row is two sweeps, unrolled so that all 18 16-byte loads of a thread are in flight together.
+// ---- shrink for small batches: one CTA per (sorted token, 8 adapter rows, 1024 features) ------
+// 128 threads each own 8 consecutive input features, so a CTA reads 2 KB of x and 16 KB of A
+// with all nine 16-byte loads of a thread in flight; the K-parts are summed by the consumers.
+constexpr int kShrKChunk = 1024;
+
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128)
 shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
-    __shared__ float red[8][8];
+    __shared__ float red[4][8];
     pdl_wait();
     pdl_trigger();
     if (*seg.status != LORA_OK) return;
-    const int j = blockIdx.x, g = blockIdx.y;
+    const int j = blockIdx.x, g = blockIdx.y, ks = blockIdx.z;
     if (j >= seg.n) return;
     const int t = seg.perm[j];
     const int s = seg.idx[t];
     if (s < 0) return;
     const int h = pool.h_in, R = pool.R;
-    const T* xr = x + (size_t)t * h;
-    const T* Ar = static_cast<const T*>(pool.A) + ((size_t)s * R + (size_t)g * 8) * h;
+    const int k = ks * kShrKChunk + threadIdx.x * 8;
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.f;
-    for (int k0 = threadIdx.x * 8; k0 < h; k0 += 2 * 2048) {
-        const int k1 = k0 + 2048;
-        const bool two = k1 < h;
-        uint4 xv0 = *reinterpret_cast<const uint4*>(xr + k0);
-        uint4 xv1 = two ? *reinterpret_cast<const uint4*>(xr + k1) : make_uint4(0, 0, 0, 0);
-        uint4 av0[8], av1[8];
+    if (k < h) {
+        const T* Ar = static_cast<const T*>(pool.A) + ((size_t)s * R + (size_t)g * 8) * h + k;
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + (size_t)t * h + k);
+        uint4 av[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) av[r] = __ldg(reinterpret_cast<const uint4*>(Ar + (size_t)r * h));
+        float xf[8];
+        unpack8<T>(xv, xf);
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-            av0[r] = __ldg(reinterpret_cast<const uint4*>(Ar + (size_t)r * h + k0));
-            av1[r] = two ? __ldg(reinterpret_cast<const uint4*>(Ar + (size_t)r * h + k1)) : make_uint4(0, 0, 0, 0);
-        }
-        float xf0[8], xf1[8];
-        unpack8<T>(xv0, xf0);
-        unpack8<T>(xv1, xf1);
+            float af[8];
+            unpack8<T>(av[r], af);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            float a0[8], a1[8];
-            unpack8<T>(av0[r], a0);
-            unpack8<T>(av1[r], a1);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[r] = fmaf(xf0[e], a0[e], fmaf(xf1[e], a1[e], acc[r]));
+            for (int e = 0; e < 8; ++e) acc[r] = fmaf(xf[e], af[e], acc[r]);
         }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -122,10 +116,8 @@ shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* 
     }
     __syncthreads();
     if (threadIdx.x < 8) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) v += red[w][threadIdx.x];
-        s_out[(size_t)t * R + g * 8 + threadIdx.x] = pool.table[s].scale * v;
+        const float v = red[0][threadIdx.x] + red[1][threadIdx.x] + red[2][threadIdx.x] + red[3][threadIdx.x];
+        s_out[((size_t)ks * seg.n + t) * R + g * 8 + threadIdx.x] = pool.table[s].scale * v;
     }
 }
 
@@ -241,7 +233,7 @@ constexpr int kExpTT = 16;
 
 template <typename T>
 __global__ void __launch_bounds__(256)
-expand_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, T* __restrict__ y) {
+expand_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, int s_parts, T* __restrict__ y) {
     extern __shared__ float ss[];  // [TT][R]
     __shared__ int sl[kExpTT];
     pdl_wait();
@@ -254,7 +246,10 @@ expand_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, T* __r
     __syncthreads();
     for (int e = threadIdx.x; e < nt * R; e += blockDim.x) {
         const int q = e / R;
-        ss[e] = sl[q] >= 0 ? s_in[(size_t)(t0 + q) * R + e % R] : 0.f;
+        float v = 0.f;
+        if (sl[q] >= 0)
+            for (int k = 0; k < s_parts; ++k) v += s_in[((size_t)k * seg.n + t0 + q) * R + e % R];
+        ss[e] = v;
     }
     __syncthreads();
     const int o = blockIdx.x * 256 + threadIdx.x;
@@ -285,7 +280,7 @@ expand_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, T* __r
 template <typename T>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(PoolView pool, SegView seg, const T* __restrict__ W, const T* __restrict__ x,
-                 const float* __restrict__ s_in, T* __restrict__ y, int fuse_lora) {
+                 const float* __restrict__ s_in, int s_parts, T* __restrict__ y, int fuse_lora) {
     __shared__ float xs[16][65];
     __shared__ float ws[16][65];
     pdl_wait();
@@ -330,9 +325,12 @@ gemm_simt_kernel(PoolView pool, SegView seg, const T* __restrict__ W, const T* _
             float v = acc[i][jj];
             if (s >= 0) {
                 const T* Br = B + ((size_t)s * h_out + o) * R;
-                const float* sr = s_in + (size_t)t * R;
                 float l = 0.f;
-                for (int j = 0; j < R; ++j) l = fmaf(sr[j], to_f32(Br[j]), l);
+                for (int j = 0; j < R; ++j) {
+                    float sj = 0.f;
+                    for (int k = 0; k < s_parts; ++k) sj += s_in[((size_t)k * n + t) * R + j];
+                    l = fmaf(sj, to_f32(Br[j]), l);
+                }
                 v += l;
             }
             y[(size_t)t * h_out + o] = from_f32<T>(v);
@@ -342,16 +340,23 @@ gemm_simt_kernel(PoolView pool, SegView seg, const T* __restrict__ W, const T* _
 
 // ---- host launchers ----------------------------------------------------------------------------
 
+int shrink_parts(const PoolView& pv, int n, bool tiled) {
+    if (pv.dtype != LORA_F32 && !tiled) return (pv.h_in + kShrKChunk - 1) / kShrKChunk;
+    (void)n;
+    return 1;
+}
+
 template <typename T>
 static int launch_shrink_t(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st,
-                           bool tiled) {
+                           bool tiled, int* s_parts) {
     const T* xp = static_cast<const T*>(x);
+    *s_parts = shrink_parts(pv, sv.n, tiled);
     if constexpr (sizeof(T) == 2) {
         if (!tiled) {
             if (sv.n == 0) return LORA_OK;
             void* args[] = {(void*)&pv, (void*)&sv, (void*)&xp, (void*)&s_out};
-            LORA_CUDA_TRY(
-                launch_pdl((const void*)shrink_token_kernel<T>, dim3(sv.n, pv.R / 8), dim3(256), 0, st, args));
+            LORA_CUDA_TRY(launch_pdl((const void*)shrink_token_kernel<T>, dim3(sv.n, pv.R / 8, *s_parts), dim3(128), 0,
+                                     st, args));
             return LORA_OK;
         }
     }
@@ -379,53 +384,55 @@ static int launch_shrink_t(const PoolView& pv, const SegView& sv, const void* x,
     return LORA_OK;
 }
 
-int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled) {
+int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled,
+                  int* s_parts) {
     switch (pv.dtype) {
-        case LORA_F32: return launch_shrink_t<float>(pv, sv, x, s_out, st, tiled);
-        case LORA_F16: return launch_shrink_t<__half>(pv, sv, x, s_out, st, tiled);
-        default: return launch_shrink_t<__nv_bfloat16>(pv, sv, x, s_out, st, tiled);
+        case LORA_F32: return launch_shrink_t<float>(pv, sv, x, s_out, st, tiled, s_parts);
+        case LORA_F16: return launch_shrink_t<__half>(pv, sv, x, s_out, st, tiled, s_parts);
+        default: return launch_shrink_t<__nv_bfloat16>(pv, sv, x, s_out, st, tiled, s_parts);
     }
 }
 
 template <typename T>
-static int launch_expand_t(const PoolView& pv, const SegView& sv, const float* s_in, void* y, cudaStream_t st) {
+static int launch_expand_t(const PoolView& pv, const SegView& sv, const float* s_in, int s_parts, void* y,
+                           cudaStream_t st) {
     if (sv.n == 0) return LORA_OK;
     T* yp = static_cast<T*>(y);
     const dim3 grid((pv.h_out + 255) / 256, (sv.n + kExpTT - 1) / kExpTT);
     const size_t smem = sizeof(float) * kExpTT * pv.R;
-    void* args[] = {(void*)&pv, (void*)&sv, (void*)&s_in, (void*)&yp};
+    void* args[] = {(void*)&pv, (void*)&sv, (void*)&s_in, (void*)&s_parts, (void*)&yp};
     LORA_CUDA_TRY(launch_pdl((const void*)expand_kernel<T>, grid, dim3(256), smem, st, args));
     return LORA_OK;
 }
 
-int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, void* y, cudaStream_t st) {
+int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, int s_parts, void* y, cudaStream_t st) {
     switch (pv.dtype) {
-        case LORA_F32: return launch_expand_t<float>(pv, sv, s_in, y, st);
-        case LORA_F16: return launch_expand_t<__half>(pv, sv, s_in, y, st);
-        default: return launch_expand_t<__nv_bfloat16>(pv, sv, s_in, y, st);
+        case LORA_F32: return launch_expand_t<float>(pv, sv, s_in, s_parts, y, st);
+        case LORA_F16: return launch_expand_t<__half>(pv, sv, s_in, s_parts, y, st);
+        default: return launch_expand_t<__nv_bfloat16>(pv, sv, s_in, s_parts, y, st);
     }
 }
 
 template <typename T>
 static int launch_gemm_simt_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
-                              void* y, bool fuse, cudaStream_t st) {
+                              int s_parts, void* y, bool fuse, cudaStream_t st) {
     if (sv.n == 0) return LORA_OK;
     const T* Wp = static_cast<const T*>(W);
     const T* xp = static_cast<const T*>(x);
     T* yp = static_cast<T*>(y);
     int f = fuse ? 1 : 0;
     const dim3 grid((pv.h_out + 63) / 64, (sv.n + 63) / 64);
-    void* args[] = {(void*)&pv, (void*)&sv, (void*)&Wp, (void*)&xp, (void*)&s_in, (void*)&yp, (void*)&f};
+    void* args[] = {(void*)&pv, (void*)&sv, (void*)&Wp, (void*)&xp, (void*)&s_in, (void*)&s_parts, (void*)&yp, (void*)&f};
     LORA_CUDA_TRY(launch_pdl((const void*)gemm_simt_kernel<T>, grid, dim3(256), 0, st, args));
     return LORA_OK;
 }
 
-int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, void* y,
-                     bool fuse, cudaStream_t st) {
+int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
+                     int s_parts, void* y, bool fuse, cudaStream_t st) {
     switch (pv.dtype) {
-        case LORA_F32: return launch_gemm_simt_t<float>(pv, sv, W, x, s_in, y, fuse, st);
-        case LORA_F16: return launch_gemm_simt_t<__half>(pv, sv, W, x, s_in, y, fuse, st);
-        default: return launch_gemm_simt_t<__nv_bfloat16>(pv, sv, W, x, s_in, y, fuse, st);
+        case LORA_F32: return launch_gemm_simt_t<float>(pv, sv, W, x, s_in, s_parts, y, fuse, st);
+        case LORA_F16: return launch_gemm_simt_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, st);
+        default: return launch_gemm_simt_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, st);
     }
 }
 
