@@ -43,6 +43,7 @@ constexpr int kThreads = 192;
 constexpr int kPrefillBN = 256;
 constexpr int kDecodeMaxN = 256;
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kLsmMaxTokens = 32;  // decode CTAs precompute the LoRA term when they own <= this many tokens
 
 struct DecodeArgs {
     PoolView pool;
@@ -112,7 +113,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int* dlist = dloc_sm + per;                                                 // [per]
     int* fidx_sm = dlist + per;                                                 // [per]
     float* S_sm = reinterpret_cast<float*>(fidx_sm + per);                      // [per][R]
-    T* Bpre = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(S_sm + (size_t)per * R + 3) & ~uintptr_t(15));
+    const bool use_lsm = per <= kLsmMaxTokens;                                   // LoRA term precomputed
+    float* L_sm = S_sm + (size_t)per * R;                                       // [per][128] if use_lsm
+    T* Bpre = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(L_sm + (use_lsm ? (size_t)per * BM : 0) + 3) &
+                                   ~uintptr_t(15));
     uint64_t* full = reinterpret_cast<uint64_t*>(
         (reinterpret_cast<uintptr_t>(Bpre + (size_t)a.dpre * BM * R) + 7) & ~uintptr_t(7));
     uint64_t* empty = full + stages;
@@ -276,59 +280,72 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 for (int u = 0; u < 8; ++u)
                     if (e0 + u * 128 < total) reinterpret_cast<uint4*>(Bpre)[e0 + u * 128] = v[u];
             }
+            named_bar_sync(1, 128);
+            // LoRA term of this thread's feature for every token of the share (pre-staged slots)
+            for (int q = 0; q < (use_lsm ? cnt : 0); ++q) {
+                const int d = dloc_sm[q];
+                float acc = 0.f;
+                if (d >= 0 && d < Dg) {
+                    const uint4* br = reinterpret_cast<const uint4*>(Bpre) + (size_t)(d * BM + row) * chunks;
+                    const float* sr = S_sm + q * R;
+                    for (int jc = 0; jc < chunks; ++jc) {
+                        float b[8];
+                        unpack8<T>(br[jc], b);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc = fmaf(b[e], sr[jc * 8 + e], acc);
+                    }
+                }
+                L_sm[q * BM + row] = acc;
+            }
+        } else if (use_lsm) {
+            for (int q = 0; q < cnt; ++q) L_sm[q * BM + row] = 0.f;
         }
-        // ---- epilogue phase B: park the partial tile in the idle pipeline stages ----
+        // ---- epilogue phase B: wait for the accumulator ----
         const bool got = mbar_wait(tmem_full, 0, flags);
         tc_fence_after();
         named_bar_sync(1, 128);
         if (et == 0) flags[1] = (got && !flags[0] && flags[3] == LORA_OK) ? 1 : 0;
         named_bar_sync(1, 128);
-        if (flags[1]) {
-            float* P = reinterpret_cast<float*>(smem);  // [n_pad][128]
-            const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-            for (int c0 = 0; c0 < a.n_pad; c0 += 16) {
-                uint32_t r[16];
-                __syncwarp();
-                tmem_ld16(taddr + c0, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) P[(c0 + c) * BM + row] = __uint_as_float(r[c]);
-            }
-        }
     }
 
     tc_fence_before();
-    cluster_sync();  // every CTA of the cluster has parked its partial tile
+    cluster_sync();  // every CTA of the cluster is past its main loop: stage buffers are free
 
-    // ---- epilogue phase C: reduce this CTA's tokens over the cluster, add LoRA, store ----
+    // ---- epilogue phase C: push partial sums to the CTA that owns each token ----
+    // Receive buffer in the stage area of every CTA: [splits][per][128] float32.
+    float* Rcv = reinterpret_cast<float*>(smem);
     if (warp >= 2 && flags[1]) {
-        float* P = reinterpret_cast<float*>(smem);
-        float* Y_sm = P + (size_t)a.n_pad * BM;  // [per][128]
-        const uint32_t p_addr = smem_u32(P) + static_cast<uint32_t>((t0 * BM + row) * 4);
-        for (int q0 = 0; q0 < cnt; q0 += 8) {  // 8 tokens x up to 8 cluster ranks of loads in flight
-            float v[8];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t rcv_addr = smem_u32(Rcv) + static_cast<uint32_t>((split * per * BM + row) * 4);
+        for (int c0 = 0; c0 < a.n_pad && c0 < n; c0 += 16) {
+            uint32_t r[16];
+            __syncwarp();
+            tmem_ld16(taddr + c0, r);
+            tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                if (c < a.splits) {
-                    const uint32_t base_c = mapa_shared(p_addr, c);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (q0 + u < cnt) v[u] += ld_dsmem_f32(base_c + static_cast<uint32_t>((q0 + u) * BM * 4));
+            for (int c = 0; c < 16; ++c) {
+                const int t = c0 + c;
+                if (t < n) {
+                    const int dst = t / per, q = t - dst * per;
+                    st_dsmem_f32(mapa_shared(rcv_addr + static_cast<uint32_t>(q * BM * 4), dst), __uint_as_float(r[c]));
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (q0 + u < cnt) Y_sm[(q0 + u) * BM + row] = v[u];
         }
-        if (a.fuse) {
-            const int D = flags[2];
-            // slots beyond the pre-staged ones are staged now, after Y_sm, in groups
-            T* Blate = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(Y_sm + (size_t)per * BM + 3) & ~uintptr_t(15));
+    }
+    tc_fence_before();
+    cluster_sync();  // all partial sums have arrived
+
+    // ---- epilogue phase D: LoRA groups not yet applied, local reduction, store ----
+    if (warp >= 2 && flags[1]) {
+        float* own = Rcv + (size_t)split * per * BM;  // this CTA's own partials: LoRA terms are added here
+        const int D = flags[2];
+        const int g_begin = use_lsm ? a.dpre : 0;  // with L_sm the pre-staged group is already applied
+        if (a.fuse && D > g_begin) {
+            T* Blate = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(Rcv + (size_t)a.splits * per * BM + 3) &
+                                            ~uintptr_t(15));
             const size_t late_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(Blate) - smem);
             const int dlate = max(1, static_cast<int>(late_bytes / ((size_t)BM * R * sizeof(T))));
-            for (int g0 = 0; g0 < D;) {
+            for (int g0 = g_begin; g0 < D;) {
                 const bool pre = g0 == 0 && a.dpre > 0;
                 const int Dg = pre ? min(D, a.dpre) : min(D - g0, dlate);
                 const T* Bg = pre ? Bpre : Blate;
@@ -368,17 +385,22 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 #pragma unroll
                         for (int e = 0; e < 8; ++e) acc = fmaf(b[e], sr[jc * 8 + e], acc);
                     }
-                    Y_sm[q * BM + row] += acc;
+                    own[q * BM + row] += acc;
                 }
                 g0 += Dg;
             }
         }
         if (o < h_out) {
             T* y = static_cast<T*>(a.y);
-            for (int q = 0; q < cnt; ++q) y[(size_t)(t0 + q) * h_out + o] = from_f32<T>(Y_sm[q * BM + row]);
+            for (int q = 0; q < cnt; ++q) {
+                float v = use_lsm ? L_sm[q * BM + row] : 0.f;
+                for (int c = 0; c < a.splits; ++c) v += Rcv[(c * per + q) * BM + row];
+                y[(size_t)(t0 + q) * h_out + o] = from_f32<T>(v);
+            }
         }
     }
-    cluster_sync();  // nobody leaves while its partial tile may still be read
+    tc_fence_before();
+    __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
 
@@ -614,24 +636,26 @@ static DecodePlan plan_decode(const PoolView& pv, int n) {
     p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
     const int per = (p.n_pad + p.splits - 1) / p.splits;
     const size_t stage_bytes = (size_t)BM * BK * 2 + (size_t)p.n_pad * BK * 2;
-    const size_t fixed = (size_t)per * 4 * 4 + (size_t)per * pv.R * 4 + 16 + 2 * 1024 /* barriers, align */;
+    // dedicated region: 4 int arrays, s [per][R], LoRA term [per][128] (small shares), barriers
+    const bool use_lsm = per <= kLsmMaxTokens;
+    const size_t fixed =
+        (size_t)per * 4 * 4 + (size_t)per * pv.R * 4 + (use_lsm ? (size_t)per * BM * 4 : 0) + 16 + 2 * 1024;
     const size_t slot_b = (size_t)BM * pv.R * 2;
     const int want = std::min(std::min(per, pv.S), 32);
     const size_t limit = 225 * 1024;
-    p.stages = 4;
+    // the stage area must also hold the receive buffer [splits][per][128] and one late B tile
+    const size_t park = (size_t)p.splits * per * BM * 4 + 16 + slot_b;
+    int min_stages = 2;
+    while ((size_t)min_stages * stage_bytes < park) ++min_stages;
+    p.stages = std::max(4, min_stages);
     p.dpre = 0;
-    for (int st = 8; st >= 4; --st) {
+    for (int st = std::max(8, min_stages); st >= std::max(3, min_stages); --st) {
         if ((size_t)st * stage_bytes + fixed > limit) continue;
         const int dp = (int)std::min<size_t>((size_t)want, (limit - st * stage_bytes - fixed) / slot_b);
-        if (dp >= want || st == 4) {
-            p.stages = st;
-            p.dpre = dp;
-            break;
-        }
+        p.stages = st;
+        p.dpre = dp;
+        if (dp >= want) break;
     }
-    // the stage area must also hold the parked partial tile, this CTA's output rows and one late B tile
-    const size_t park = (size_t)p.n_pad * BM * 4 + (size_t)per * BM * 4 + 16 + slot_b;
-    while ((size_t)p.stages * stage_bytes < park) ++p.stages;
     int cols = 32;
     while (cols < p.n_pad) cols <<= 1;
     p.tmem_cols = cols;
