@@ -53,6 +53,7 @@ struct DecodeArgs {
     int n, n_pad, kb_total, splits, kb_per_split, stages, tmem_cols, fuse, bf16;
     int s_parts;  // K-parts of the shrink output to sum
     int dpre;     // distinct slots whose B rows are staged during the main loop
+    int push;     // exchange partials by bulk copies (1) or remote loads (0)
 };
 
 struct PrefillArgs {
@@ -87,14 +88,17 @@ __device__ __forceinline__ float lora_term(const T* __restrict__ Brow, const flo
 // ============================================================================================
 // decode: swap-AB + split-K over a thread-block cluster
 // ============================================================================================
-// The `splits` CTAs that share one 128-feature tile form a cluster (cluster dims 1 x splits).
-// While the MMA warp streams W, the epilogue warps already stage everything the LoRA term needs
-// for this CTA's share of tokens (slot ids, the distinct slots, s summed over its K-parts, and
-// the B rows of those slots) into a dedicated shared-memory region.  After its K range every
-// CTA parks its float32 partial tile [n_pad tokens][128 features] in the (then idle) pipeline
-// stages; after a cluster barrier CTA r sums the partials of tokens [r*per, (r+1)*per) over the
-// cluster through distributed shared memory, adds the LoRA term and writes y.  No global
-// scratch, no atomics.
+// The `splits` CTAs that share one 128-feature tile form a cluster (cluster dims 1 x splits);
+// CTA r owns the reduction of tokens [r*per, r*per + per).
+//  phase A (epilogue warps, overlapping the main loop): the slot ids of the owned tokens, their
+//          distinct slots, and -- by bulk copies -- the B rows of those slots for this feature
+//          tile and the owned tokens' shrink output; then the LoRA term of every owned
+//          (token, feature) pair.
+//  phase B: the float32 partial tile [n_pad tokens][128 features] is parked in the idle stages.
+//  phase C: after a cluster barrier, each CTA bulk-copies the partial rows of the tokens another
+//          CTA owns into that CTA's receive buffer (completion on the receiver's mbarrier); when
+//          the buffers do not fit, owners read the partials remotely instead.
+//  phase D: owners add the partials, the LoRA term and store y.  No global scratch.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -107,27 +111,39 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const uint32_t stage_bytes = w_bytes + x_bytes;
     const int R = a.pool.R;
     const int per = (a.n_pad + a.splits - 1) / a.splits;  // tokens reduced by each CTA
-    // dedicated LoRA staging region after the stages
+    const bool use_lsm = per <= kLsmMaxTokens;
+    // dedicated region after the stages (layout mirrored by plan_decode)
     int* slot_sm = reinterpret_cast<int*>(smem + (size_t)stages * stage_bytes);  // [per]
     int* dloc_sm = slot_sm + per;                                               // [per]
     int* dlist = dloc_sm + per;                                                 // [per]
     int* fidx_sm = dlist + per;                                                 // [per]
-    float* S_sm = reinterpret_cast<float*>(fidx_sm + per);                      // [per][R]
-    const bool use_lsm = per <= kLsmMaxTokens;                                   // LoRA term precomputed
-    float* L_sm = S_sm + (size_t)per * R;                                       // [per][128] if use_lsm
+    float* S_sm = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(fidx_sm + per) + 15) & ~uintptr_t(15));  // [s_parts][per][R]
+    float* L_sm = S_sm + (size_t)a.s_parts * per * R;                            // [per][128] if use_lsm
     T* Bpre = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(L_sm + (use_lsm ? (size_t)per * BM : 0) + 3) &
-                                   ~uintptr_t(15));
+                                   ~uintptr_t(15));  // [dpre][128][R]
     uint64_t* full = reinterpret_cast<uint64_t*>(
         (reinterpret_cast<uintptr_t>(Bpre + (size_t)a.dpre * BM * R) + 7) & ~uintptr_t(7));
     uint64_t* empty = full + stages;
     uint64_t* tmem_full = empty + stages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+    uint64_t* lbar = tmem_full + 1;  // LoRA operands staged
+    uint64_t* rbar = lbar + 1;       // partial rows received
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 1);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort, go, D, status, wsum[4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, split = blockIdx.y;
     const int kb0 = split * a.kb_per_split;
     const int nkb = min(a.kb_total, kb0 + a.kb_per_split) - kb0;
+    const int n = a.n, h_out = a.pool.h_out;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int t0 = rank * per;
+    const int cnt = max(0, min(n, t0 + per) - t0);
+    const int rows_valid = min(BM, h_out - m_tile * BM);
+    // stage area after the main loop: P [n_pad][128] | Rcv [splits][per][128] | late B tiles
+    float* P = reinterpret_cast<float*>(smem);
+    float* Rcv = P + (size_t)a.n_pad * BM;
+    const bool push = a.push != 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -135,6 +151,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             mbar_init(&empty[s], 1);
         }
         mbar_init(tmem_full, 1);
+        mbar_init(lbar, 1);
+        mbar_init(rbar, 1);
         for (int i = 0; i < 8; ++i) flags[i] = 0;
         fence_barrier_init();
     }
@@ -155,22 +173,25 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int et = threadIdx.x - 64;  // 0..127 in the epilogue warps
     const int row = (warp & 3) * 32 + lane;
     const int o = m_tile * BM + row;
-    const int h_out = a.pool.h_out, n = a.n;
-    const int rank = static_cast<int>(cluster_ctarank());
-    const int t0 = rank * per;
-    const int cnt = max(0, min(n, t0 + per) - t0);
     const int chunks = R / 8;  // 16-byte chunks per B row
     const T* B = static_cast<const T*>(a.pool.B);
 
     if (warp == 0) {
         if (lane == 0) {
-            // x is complete before this grid starts: the preceding shrink kernel releases its
-            // dependents only after its own grid-dependency wait.
-            int issued = 0;
-            for (int i = 0; i < nkb; ++i) {
+            // W does not depend on earlier kernels: the first ring pass loads W tiles at once;
+            // x is read after the grid-dependency wait (it may be the previous layer's output).
+            const int pre = min(stages, nkb);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], stage_bytes);
+                tma_load_2d(smem + i * stage_bytes, &tmW, &full[i], (kb0 + i) * BK, m_tile * BM);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(smem + i * stage_bytes + w_bytes, &tmX, &full[i], (kb0 + i) * BK, 0);
+            int issued = pre;
+            for (int i = pre; i < nkb; ++i) {
                 const int s = i % stages;
-                const uint32_t ph = (i / stages) & 1;
-                if (i >= stages && !mbar_wait(&empty[s], ph ^ 1, flags)) break;
+                if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tma_load_2d(smem + s * stage_bytes, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM);
                 tma_load_2d(smem + s * stage_bytes + w_bytes, &tmX, &full[s], (kb0 + i) * BK, 0);
@@ -206,11 +227,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             umma_commit(tmem_full);  // also on abort: fires once the issued MMAs have finished
         }
     } else {
-        // ---- epilogue phase A (overlaps the main loop): stage this CTA's LoRA operands ----
+        // ---- phase A (overlaps the main loop): stage this CTA's LoRA operands ----
         pdl_wait();  // s, idx and the status word come from earlier kernels
         if (et == 0) flags[3] = __ldcg(a.seg.status);
         named_bar_sync(1, 128);
-        if (flags[3] == LORA_OK && a.fuse) {
+        const bool lora = flags[3] == LORA_OK && a.fuse;
+        if (lora) {
             for (int q = et; q < cnt; q += 128) slot_sm[q] = __ldcg(a.seg.idx + t0 + q);
             named_bar_sync(1, 128);
             // distinct slots of this CTA's tokens: dloc_sm[q] = index of token q's slot in dlist
@@ -244,105 +266,109 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 }
                 running += wsum[0] + wsum[1] + wsum[2] + wsum[3];
             }
-            if (et == 0) flags[2] = running;
             named_bar_sync(1, 128);
             for (int q = et; q < cnt; q += 128) {
                 const int f = fidx_sm[q];
                 if (f != q) dloc_sm[q] = f >= 0 ? dloc_sm[f] : -1;
             }
-            // s of this CTA's tokens, summed over the shrink's K-parts
-            for (int e = et; e < cnt * R; e += 128) {
-                const int q = e / R, j = e - q * R;
-                float v = 0.f;
-                if (slot_sm[q] >= 0)
-                    for (int k = 0; k < a.s_parts; ++k) v += __ldcg(a.s_in + ((size_t)k * n + t0 + q) * R + j);
-                S_sm[e] = v;
-            }
-            // B rows of the first dpre distinct slots
             const int Dg = min(running, a.dpre);
-            const int total = Dg * BM * chunks;
-            for (int e0 = et; e0 < total; e0 += 8 * 128) {
-                uint4 v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int e = e0 + u * 128;
-                    v[u] = make_uint4(0, 0, 0, 0);
-                    if (e < total) {
-                        const int d = e / (BM * chunks);
-                        const int rem = e - d * (BM * chunks);
-                        const int oo = m_tile * BM + rem / chunks;
-                        if (oo < h_out)
-                            v[u] = __ldg(reinterpret_cast<const uint4*>(B + ((size_t)dlist[d] * h_out + oo) * R +
-                                                                         (rem % chunks) * 8));
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (e0 + u * 128 < total) reinterpret_cast<uint4*>(Bpre)[e0 + u * 128] = v[u];
+            if (et == 0) {
+                flags[2] = running;
+                // bulk copies: the owned tokens' shrink parts, then the pre-staged slots' B rows
+                const uint32_t s_bytes = static_cast<uint32_t>(cnt * R * 4);
+                const uint32_t b_bytes = static_cast<uint32_t>(rows_valid * R * 2);
+                const uint32_t total = (cnt > 0 ? a.s_parts * s_bytes : 0) + Dg * b_bytes;
+                mbar_arrive_expect_tx(lbar, total);
+                if (cnt > 0)
+                    for (int k = 0; k < a.s_parts; ++k)
+                        bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
+                for (int d = 0; d < Dg; ++d)
+                    bulk_g2s(Bpre + (size_t)d * BM * R, B + ((size_t)dlist[d] * h_out + m_tile * BM) * R, b_bytes,
+                             lbar);
             }
             named_bar_sync(1, 128);
-            // LoRA term of this thread's feature for every token of the share (pre-staged slots)
-            for (int q = 0; q < (use_lsm ? cnt : 0); ++q) {
-                const int d = dloc_sm[q];
-                float acc = 0.f;
-                if (d >= 0 && d < Dg) {
-                    const uint4* br = reinterpret_cast<const uint4*>(Bpre) + (size_t)(d * BM + row) * chunks;
-                    const float* sr = S_sm + q * R;
-                    for (int jc = 0; jc < chunks; ++jc) {
-                        float b[8];
-                        unpack8<T>(br[jc], b);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc = fmaf(b[e], sr[jc * 8 + e], acc);
+            const bool staged = mbar_wait(lbar, 0, flags);
+            // LoRA term of this thread's feature for every owned token whose slot is pre-staged
+            if (use_lsm) {
+                for (int q = 0; q < cnt; ++q) {
+                    const int d = dloc_sm[q];
+                    float acc = 0.f;
+                    if (staged && d >= 0 && d < Dg) {
+                        const uint4* br = reinterpret_cast<const uint4*>(Bpre) + (size_t)(d * BM + row) * chunks;
+                        for (int k = 0; k < a.s_parts; ++k) {
+                            const float* sr = S_sm + ((size_t)k * per + q) * R;
+                            for (int jc = 0; jc < chunks; ++jc) {
+                                float b[8];
+                                unpack8<T>(br[jc], b);
+                                const float4 s0 = reinterpret_cast<const float4*>(sr + jc * 8)[0];
+                                const float4 s1 = reinterpret_cast<const float4*>(sr + jc * 8)[1];
+                                acc = fmaf(b[0], s0.x, acc);
+                                acc = fmaf(b[1], s0.y, acc);
+                                acc = fmaf(b[2], s0.z, acc);
+                                acc = fmaf(b[3], s0.w, acc);
+                                acc = fmaf(b[4], s1.x, acc);
+                                acc = fmaf(b[5], s1.y, acc);
+                                acc = fmaf(b[6], s1.z, acc);
+                                acc = fmaf(b[7], s1.w, acc);
+                            }
+                        }
                     }
+                    L_sm[q * BM + row] = acc;
                 }
-                L_sm[q * BM + row] = acc;
             }
         } else if (use_lsm) {
             for (int q = 0; q < cnt; ++q) L_sm[q * BM + row] = 0.f;
         }
-        // ---- epilogue phase B: wait for the accumulator ----
+        // ---- phase B: park the partial tile in the idle stages ----
         const bool got = mbar_wait(tmem_full, 0, flags);
         tc_fence_after();
         named_bar_sync(1, 128);
-        if (et == 0) flags[1] = (got && !flags[0] && flags[3] == LORA_OK) ? 1 : 0;
+        if (et == 0) {
+            flags[1] = (got && !flags[0] && flags[3] == LORA_OK) ? 1 : 0;
+            // receive buffer: one bulk copy of this CTA's token rows from every other CTA
+            if (push && flags[1] && cnt > 0) mbar_arrive_expect_tx(rbar, (uint32_t)((a.splits - 1) * cnt * BM * 4));
+        }
         named_bar_sync(1, 128);
-    }
-
-    tc_fence_before();
-    cluster_sync();  // every CTA of the cluster is past its main loop: stage buffers are free
-
-    // ---- epilogue phase C: push partial sums to the CTA that owns each token ----
-    // Receive buffer in the stage area of every CTA: [splits][per][128] float32.
-    float* Rcv = reinterpret_cast<float*>(smem);
-    if (warp >= 2 && flags[1]) {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const uint32_t rcv_addr = smem_u32(Rcv) + static_cast<uint32_t>((split * per * BM + row) * 4);
-        for (int c0 = 0; c0 < a.n_pad && c0 < n; c0 += 16) {
-            uint32_t r[16];
-            __syncwarp();
-            tmem_ld16(taddr + c0, r);
-            tmem_ld_wait();
+        if (flags[1]) {
+            const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            for (int c0 = 0; c0 < a.n_pad && c0 < n; c0 += 16) {
+                uint32_t r[16];
+                __syncwarp();
+                tmem_ld16(taddr + c0, r);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int t = c0 + c;
-                if (t < n) {
-                    const int dst = t / per, q = t - dst * per;
-                    st_dsmem_f32(mapa_shared(rcv_addr + static_cast<uint32_t>(q * BM * 4), dst), __uint_as_float(r[c]));
-                }
+                for (int c = 0; c < 16; ++c) P[(c0 + c) * BM + row] = __uint_as_float(r[c]);
             }
+            fence_proxy_async_smem();  // the parked rows are read by bulk copies
         }
     }
-    tc_fence_before();
-    cluster_sync();  // all partial sums have arrived
 
-    // ---- epilogue phase D: LoRA groups not yet applied, local reduction, store ----
+    tc_fence_before();
+    cluster_sync();  // every CTA of the cluster is past its main loop and has parked its partials
+
+    // ---- phase C: send the partial rows of tokens owned by other CTAs ----
+    if (push && threadIdx.x == 64 && flags[1]) {
+        for (int dst = 0; dst < a.splits; ++dst) {
+            if (dst == rank) continue;
+            const int dt0 = dst * per;
+            const int dcnt = max(0, min(n, dt0 + per) - dt0);
+            if (dcnt == 0) continue;
+            const int slot_idx = rank < dst ? rank : rank - 1;  // sender index in dst's buffer
+            const uint32_t dst_addr =
+                mapa_shared(smem_u32(Rcv + (size_t)slot_idx * per * BM), static_cast<uint32_t>(dst));
+            const uint32_t dst_bar = mapa_shared(smem_u32(rbar), static_cast<uint32_t>(dst));
+            bulk_s2cluster(dst_addr, P + (size_t)dt0 * BM, static_cast<uint32_t>(dcnt * BM * 4), dst_bar);
+        }
+    }
+
+    // ---- phase D: late LoRA groups, reduction over the cluster, store ----
     if (warp >= 2 && flags[1]) {
-        float* own = Rcv + (size_t)split * per * BM;  // this CTA's own partials: LoRA terms are added here
+        float* own = P + (size_t)t0 * BM;  // this CTA's partials of its own tokens (LoRA added here)
         const int D = flags[2];
         const int g_begin = use_lsm ? a.dpre : 0;  // with L_sm the pre-staged group is already applied
         if (a.fuse && D > g_begin) {
-            T* Blate = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(Rcv + (size_t)a.splits * per * BM + 3) &
-                                            ~uintptr_t(15));
+            T* Blate = reinterpret_cast<T*>(
+                reinterpret_cast<uintptr_t>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0) + 3) & ~uintptr_t(15));
             const size_t late_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(Blate) - smem);
             const int dlate = max(1, static_cast<int>(late_bytes / ((size_t)BM * R * sizeof(T))));
             for (int g0 = g_begin; g0 < D;) {
@@ -377,30 +403,52 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const int d = dloc_sm[q] - g0;
                     if (d < 0 || d >= Dg) continue;
                     const uint4* br = reinterpret_cast<const uint4*>(Bg) + (size_t)(d * BM + row) * chunks;
-                    const float* sr = S_sm + q * R;
                     float acc = 0.f;
-                    for (int jc = 0; jc < chunks; ++jc) {
-                        float b[8];
-                        unpack8<T>(br[jc], b);
+                    for (int k = 0; k < a.s_parts; ++k) {
+                        const float* sr = S_sm + ((size_t)k * per + q) * R;
+                        for (int jc = 0; jc < chunks; ++jc) {
+                            float b[8];
+                            unpack8<T>(br[jc], b);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc = fmaf(b[e], sr[jc * 8 + e], acc);
+                            for (int e = 0; e < 8; ++e) acc = fmaf(b[e], sr[jc * 8 + e], acc);
+                        }
                     }
                     own[q * BM + row] += acc;
                 }
                 g0 += Dg;
             }
         }
-        if (o < h_out) {
+        bool recv = true;
+        if (push && cnt > 0 && a.splits > 1) recv = __all_sync(0xffffffffu, mbar_wait(rbar, 0, flags));
+        if (recv && o < h_out) {
             T* y = static_cast<T*>(a.y);
-            for (int q = 0; q < cnt; ++q) {
-                float v = use_lsm ? L_sm[q * BM + row] : 0.f;
-                for (int c = 0; c < a.splits; ++c) v += Rcv[(c * per + q) * BM + row];
-                y[(size_t)(t0 + q) * h_out + o] = from_f32<T>(v);
+            const uint32_t p_addr = smem_u32(own + row);
+            for (int q0 = 0; q0 < cnt; q0 += 4) {
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int q = q0 + u;
+                    v[u] = 0.f;
+                    if (q < cnt) {
+                        v[u] = own[q * BM + row] + (use_lsm ? L_sm[q * BM + row] : 0.f);
+                        if (push) {
+                            for (int c = 0; c < a.splits - 1; ++c) v[u] += Rcv[((size_t)c * per + q) * BM + row];
+                        } else {
+                            for (int c = 0; c < a.splits; ++c)
+                                if (c != rank)
+                                    v[u] += ld_dsmem_f32(mapa_shared(p_addr + static_cast<uint32_t>(q * BM * 4),
+                                                                     static_cast<uint32_t>(c)));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (q0 + u < cnt) y[(size_t)(t0 + q0 + u) * h_out + o] = from_f32<T>(v[u]);
             }
         }
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // no CTA leaves while its parked rows may still be copied or read
     if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
 
@@ -619,12 +667,14 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 // ============================================================================================
 
 struct DecodePlan {
-    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre;
+    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre, push, s_parts;
     size_t smem;
 };
 
-static DecodePlan plan_decode(const PoolView& pv, int n) {
+// Shared-memory plan of gemm_decode_kernel (its layout comments are the reference).
+static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     DecodePlan p;
+    p.s_parts = s_parts;
     p.n_pad = std::max(16, (n + 15) / 16 * 16);
     p.m_tiles = (pv.h_out + BM - 1) / BM;
     p.kb_total = (pv.h_in + BK - 1) / BK;
@@ -636,26 +686,35 @@ static DecodePlan plan_decode(const PoolView& pv, int n) {
     p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
     const int per = (p.n_pad + p.splits - 1) / p.splits;
     const size_t stage_bytes = (size_t)BM * BK * 2 + (size_t)p.n_pad * BK * 2;
-    // dedicated region: 4 int arrays, s [per][R], LoRA term [per][128] (small shares), barriers
     const bool use_lsm = per <= kLsmMaxTokens;
-    const size_t fixed =
-        (size_t)per * 4 * 4 + (size_t)per * pv.R * 4 + (use_lsm ? (size_t)per * BM * 4 : 0) + 16 + 2 * 1024;
+    // dedicated region: 4 int arrays, s parts [s_parts][per][R], LoRA term [per][128] (small
+    // shares), alignment, barriers
+    const size_t fixed = (size_t)per * 4 * 4 + 16 + (size_t)s_parts * per * pv.R * 4 +
+                         (use_lsm ? (size_t)per * BM * 4 : 0) + 16 + 2 * 1024;
     const size_t slot_b = (size_t)BM * pv.R * 2;
     const int want = std::min(std::min(per, pv.S), 32);
     const size_t limit = 225 * 1024;
-    // the stage area must also hold the receive buffer [splits][per][128] and one late B tile
-    const size_t park = (size_t)p.splits * per * BM * 4 + 16 + slot_b;
-    int min_stages = 2;
-    while ((size_t)min_stages * stage_bytes < park) ++min_stages;
-    p.stages = std::max(4, min_stages);
+    // stage area after the main loop: P [n_pad][128] + receive buffer [splits-1][per][128]
+    // (exchange by bulk copies) + one late B tile
+    const size_t park_push = (size_t)p.n_pad * BM * 4 + (size_t)(p.splits - 1) * per * BM * 4 + 16 + slot_b;
+    const size_t park_pull = (size_t)p.n_pad * BM * 4 + 16 + slot_b;
+    p.push = 1;
+    p.stages = 0;
     p.dpre = 0;
-    for (int st = std::max(8, min_stages); st >= std::max(3, min_stages); --st) {
-        if ((size_t)st * stage_bytes + fixed > limit) continue;
-        const int dp = (int)std::min<size_t>((size_t)want, (limit - st * stage_bytes - fixed) / slot_b);
-        p.stages = st;
-        p.dpre = dp;
-        if (dp >= want) break;
+    for (int pass = 0; pass < 2 && !p.stages; ++pass) {
+        const size_t park = pass == 0 ? park_push : park_pull;
+        int min_stages = 2;
+        while ((size_t)min_stages * stage_bytes < park) ++min_stages;
+        for (int st = std::max(8, min_stages); st >= std::max(3, min_stages); --st) {
+            if ((size_t)st * stage_bytes + fixed > limit) continue;
+            const int dp = (int)std::min<size_t>((size_t)want, (limit - st * stage_bytes - fixed) / slot_b);
+            p.stages = st;
+            p.dpre = dp;
+            p.push = pass == 0;
+            if (dp >= want) break;
+        }
     }
+    if (!p.stages) p.stages = 8;  // does not fit: tc_supported rejects the shape
     int cols = 32;
     while (cols < p.n_pad) cols <<= 1;
     p.tmem_cols = cols;
@@ -668,7 +727,8 @@ static DecodePlan plan_decode(const PoolView& pv, int n) {
 int tc_supported(const PoolView& pv, int n) {
     if (pv.dtype != LORA_F16 && pv.dtype != LORA_BF16) return 0;
     if (pv.h_in % 8 || pv.h_out % 8 || pv.R % 8) return 0;
-    if (n > 0 && n <= tc::kDecodeMaxN && tc::plan_decode(pv, n).smem > (size_t)(227 * 1024)) return 0;
+    if (n > 0 && n <= tc::kDecodeMaxN && tc::plan_decode(pv, n, (pv.h_in + 1023) / 1024).smem > (size_t)(227 * 1024))
+        return 0;
     return 1;
 }
 
@@ -680,7 +740,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     if (n == 0) return LORA_OK;
     const int bf16 = pv.dtype == LORA_BF16;
     if (n <= kDecodeMaxN) {
-        const DecodePlan p = plan_decode(pv, n);
+        const DecodePlan p = plan_decode(pv, n, s_parts);
         CUtensorMap mW, mX;
         int rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, BM);
         if (rc) return rc;
@@ -702,6 +762,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.bf16 = bf16;
         a.s_parts = s_parts;
         a.dpre = p.dpre;
+        a.push = p.push;
         static bool attr_set = false;
         if (!attr_set) {
             LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,

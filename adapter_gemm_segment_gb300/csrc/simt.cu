@@ -70,31 +70,33 @@ shrink_warp_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* _
     }
 }
 
-// ---- shrink for small batches: one CTA per (sorted token, 8 adapter rows, 1024 features) ------
+// ---- shrink for small batches: one CTA per (token, 8 adapter rows, 1024 features) -------------
 // 128 threads each own 8 consecutive input features, so a CTA reads 2 KB of x and 16 KB of A
 // with all nine 16-byte loads of a thread in flight; the K-parts are summed by the consumers.
+// The whole grid is resident at once for decode batches, so tokens are taken in their original
+// order (one dependent load less than walking the sorted order).
 constexpr int kShrKChunk = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(128)
 shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
     __shared__ float red[4][8];
+    pdl_trigger();  // dependents wait for this grid's completion before reading s
     pdl_wait();
-    pdl_trigger();
-    if (*seg.status != LORA_OK) return;
-    const int j = blockIdx.x, g = blockIdx.y, ks = blockIdx.z;
-    if (j >= seg.n) return;
-    const int t = seg.perm[j];
-    const int s = seg.idx[t];
-    if (s < 0) return;
+    const int t = blockIdx.x, g = blockIdx.y, ks = blockIdx.z;
     const int h = pool.h_in, R = pool.R;
     const int k = ks * kShrKChunk + threadIdx.x * 8;
+    // independent loads first: status, slot, x; then the slot's A rows
+    const int status = __ldcg(seg.status);
+    const int s = __ldcg(seg.idx + t);
+    uint4 xv = make_uint4(0, 0, 0, 0);
+    if (k < h) xv = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * h + k));
+    if (s < 0 || status != LORA_OK) return;
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.f;
     if (k < h) {
         const T* Ar = static_cast<const T*>(pool.A) + ((size_t)s * R + (size_t)g * 8) * h + k;
-        const uint4 xv = *reinterpret_cast<const uint4*>(x + (size_t)t * h + k);
         uint4 av[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) av[r] = __ldg(reinterpret_cast<const uint4*>(Ar + (size_t)r * h));
@@ -108,6 +110,7 @@ shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* 
             for (int e = 0; e < 8; ++e) acc[r] = fmaf(xf[e], af[e], acc[r]);
         }
     }
+    const float scale = pool.table[s].scale;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -117,7 +120,7 @@ shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* 
     __syncthreads();
     if (threadIdx.x < 8) {
         const float v = red[0][threadIdx.x] + red[1][threadIdx.x] + red[2][threadIdx.x] + red[3][threadIdx.x];
-        s_out[((size_t)ks * seg.n + t) * R + g * 8 + threadIdx.x] = pool.table[s].scale * v;
+        s_out[((size_t)ks * seg.n + t) * R + g * 8 + threadIdx.x] = scale * v;
     }
 }
 

@@ -96,6 +96,26 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Bulk (non-tensor) copies: global -> own shared memory, and own shared memory -> the shared
+// memory of another CTA of the cluster; both complete on an mbarrier in the destination CTA.
+// Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster_addr, const void* src, uint32_t bytes,
+                                               uint32_t bar_cluster_addr) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster_addr),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster_addr)
+        : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---- tcgen05: tensor memory ------------------------------------------------------------------------
 // Whole-warp instructions.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
