@@ -85,6 +85,31 @@ __device__ __forceinline__ float lora_term(const T* __restrict__ Brow, const flo
     return acc;
 }
 
+// dot(B row of one feature, s row of one token) over r_max, both in shared memory.  Lanes walk
+// the 16-byte chunks of their rows in a staggered order so that a warp whose lanes read
+// consecutive B rows (row pitch r_max*2 bytes) hits distinct banks for any r_max.
+template <typename T>
+__device__ __forceinline__ float lora_dot_smem(const uint4* __restrict__ br, const float* __restrict__ sr, int chunks,
+                                               int lane) {
+    float acc = 0.f;
+    for (int jj = 0; jj < chunks; ++jj) {
+        const int jc = (jj + lane) % chunks;
+        float b[8];
+        unpack8<T>(br[jc], b);
+        const float4 s0 = reinterpret_cast<const float4*>(sr + jc * 8)[0];
+        const float4 s1 = reinterpret_cast<const float4*>(sr + jc * 8)[1];
+        acc = fmaf(b[0], s0.x, acc);
+        acc = fmaf(b[1], s0.y, acc);
+        acc = fmaf(b[2], s0.z, acc);
+        acc = fmaf(b[3], s0.w, acc);
+        acc = fmaf(b[4], s1.x, acc);
+        acc = fmaf(b[5], s1.y, acc);
+        acc = fmaf(b[6], s1.z, acc);
+        acc = fmaf(b[7], s1.w, acc);
+    }
+    return acc;
+}
+
 // ============================================================================================
 // decode: swap-AB + split-K over a thread-block cluster
 // ============================================================================================
@@ -104,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
     const uint32_t w_bytes = BM * BK * 2;
     const uint32_t x_bytes = static_cast<uint32_t>(a.n_pad) * BK * 2;
@@ -117,13 +142,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int* dloc_sm = slot_sm + per;                                               // [per]
     int* dlist = dloc_sm + per;                                                 // [per]
     int* fidx_sm = dlist + per;                                                 // [per]
-    float* S_sm = reinterpret_cast<float*>(
-        (reinterpret_cast<uintptr_t>(fidx_sm + per) + 15) & ~uintptr_t(15));  // [s_parts][per][R]
+    float* S_sm = smem_align(reinterpret_cast<float*>(fidx_sm + per), 16);      // [s_parts][per][R]
     float* L_sm = S_sm + (size_t)a.s_parts * per * R;                            // [per][128] if use_lsm
-    T* Bpre = reinterpret_cast<T*>(reinterpret_cast<uintptr_t>(L_sm + (use_lsm ? (size_t)per * BM : 0) + 3) &
-                                   ~uintptr_t(15));  // [dpre][128][R]
-    uint64_t* full = reinterpret_cast<uint64_t*>(
-        (reinterpret_cast<uintptr_t>(Bpre + (size_t)a.dpre * BM * R) + 7) & ~uintptr_t(7));
+    T* Bpre = smem_align(reinterpret_cast<T*>(L_sm + (use_lsm ? (size_t)per * BM : 0)), 16);  // [dpre][128][R]
+    uint64_t* full = smem_align(reinterpret_cast<uint64_t*>(Bpre + (size_t)a.dpre * BM * R), 8);
     uint64_t* empty = full + stages;
     uint64_t* tmem_full = empty + stages;
     uint64_t* lbar = tmem_full + 1;  // LoRA operands staged
@@ -288,31 +310,21 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
             named_bar_sync(1, 128);
             const bool staged = mbar_wait(lbar, 0, flags);
+            // sum the shrink's K-parts once (part 0 receives the total)
+            for (int e = et; e < cnt * R; e += 128) {
+                float v = S_sm[e];
+                for (int k = 1; k < a.s_parts; ++k) v += S_sm[(size_t)k * per * R + e];
+                S_sm[e] = v;
+            }
+            named_bar_sync(1, 128);
             // LoRA term of this thread's feature for every owned token whose slot is pre-staged
             if (use_lsm) {
                 for (int q = 0; q < cnt; ++q) {
                     const int d = dloc_sm[q];
                     float acc = 0.f;
-                    if (staged && d >= 0 && d < Dg) {
-                        const uint4* br = reinterpret_cast<const uint4*>(Bpre) + (size_t)(d * BM + row) * chunks;
-                        for (int k = 0; k < a.s_parts; ++k) {
-                            const float* sr = S_sm + ((size_t)k * per + q) * R;
-                            for (int jc = 0; jc < chunks; ++jc) {
-                                float b[8];
-                                unpack8<T>(br[jc], b);
-                                const float4 s0 = reinterpret_cast<const float4*>(sr + jc * 8)[0];
-                                const float4 s1 = reinterpret_cast<const float4*>(sr + jc * 8)[1];
-                                acc = fmaf(b[0], s0.x, acc);
-                                acc = fmaf(b[1], s0.y, acc);
-                                acc = fmaf(b[2], s0.z, acc);
-                                acc = fmaf(b[3], s0.w, acc);
-                                acc = fmaf(b[4], s1.x, acc);
-                                acc = fmaf(b[5], s1.y, acc);
-                                acc = fmaf(b[6], s1.z, acc);
-                                acc = fmaf(b[7], s1.w, acc);
-                            }
-                        }
-                    }
+                    if (staged && d >= 0 && d < Dg)
+                        acc = lora_dot_smem<T>(reinterpret_cast<const uint4*>(Bpre) + (size_t)(d * BM + row) * chunks,
+                                               S_sm + q * R, chunks, lane);
                     L_sm[q * BM + row] = acc;
                 }
             }
@@ -367,8 +379,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int D = flags[2];
         const int g_begin = use_lsm ? a.dpre : 0;  // with L_sm the pre-staged group is already applied
         if (a.fuse && D > g_begin) {
-            T* Blate = reinterpret_cast<T*>(
-                reinterpret_cast<uintptr_t>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0) + 3) & ~uintptr_t(15));
+            T* Blate = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 16);
             const size_t late_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(Blate) - smem);
             const int dlate = max(1, static_cast<int>(late_bytes / ((size_t)BM * R * sizeof(T))));
             for (int g0 = g_begin; g0 < D;) {
@@ -402,18 +413,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 for (int q = 0; q < cnt; ++q) {
                     const int d = dloc_sm[q] - g0;
                     if (d < 0 || d >= Dg) continue;
-                    const uint4* br = reinterpret_cast<const uint4*>(Bg) + (size_t)(d * BM + row) * chunks;
-                    float acc = 0.f;
-                    for (int k = 0; k < a.s_parts; ++k) {
-                        const float* sr = S_sm + ((size_t)k * per + q) * R;
-                        for (int jc = 0; jc < chunks; ++jc) {
-                            float b[8];
-                            unpack8<T>(br[jc], b);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc = fmaf(b[e], sr[jc * 8 + e], acc);
-                        }
-                    }
-                    own[q * BM + row] += acc;
+                    own[q * BM + row] += lora_dot_smem<T>(reinterpret_cast<const uint4*>(Bg) + (size_t)(d * BM + row) * chunks,
+                                                          S_sm + q * R, chunks, lane);
                 }
                 g0 += Dg;
             }
@@ -461,7 +462,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     const PrefillArgs a) {
     constexpr int BN = kPrefillBN;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
     constexpr uint32_t x_bytes = BM * BK * 2;
     constexpr uint32_t w_bytes = BN * BK * 2;

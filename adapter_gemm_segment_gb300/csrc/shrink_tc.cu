@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kShrThreads, 1)
 shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA,
                  const ShrinkArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = smem_align(smem_raw, 1024);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kShrStages * kShrStageBytes);
     uint64_t* empty = full + kShrStages;
     uint64_t* acc_full = empty + kShrStages;  // [2]

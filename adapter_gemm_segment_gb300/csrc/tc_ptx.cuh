@@ -14,6 +14,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Round a shared-memory pointer up to `align` (a power of two) bytes by pointer arithmetic, so
+// that the compiler still knows it points to shared memory (a round trip through an integer
+// would turn every access into a slower generic one).
+template <typename P>
+__device__ __forceinline__ P* smem_align(P* p, uint32_t align) {
+    const uint32_t pad = (align - (smem_u32(p) & (align - 1))) & (align - 1);
+    return reinterpret_cast<P*>(reinterpret_cast<uint8_t*>(p) + pad);
+}
+
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
