@@ -127,7 +127,7 @@ __device__ __forceinline__ float lora_dot_smem(const uint4* __restrict__ br, con
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const DecodeArgs a) {
+                   const __grid_constant__ CUtensorMap tmY, const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
@@ -181,6 +181,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
+        prefetch_tmap(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, a.tmem_cols);
@@ -200,20 +201,13 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     if (warp == 0) {
         if (lane == 0) {
-            // W does not depend on earlier kernels: the first ring pass loads W tiles at once;
-            // x is read after the grid-dependency wait (it may be the previous layer's output).
-            const int pre = min(stages, nkb);
-            for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], stage_bytes);
-                tma_load_2d(smem + i * stage_bytes, &tmW, &full[i], (kb0 + i) * BK, m_tile * BM);
-            }
-            pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem + i * stage_bytes + w_bytes, &tmX, &full[i], (kb0 + i) * BK, 0);
-            int issued = pre;
-            for (int i = pre; i < nkb; ++i) {
+            // W and x are complete when this grid starts: the shrink kernel that precedes it in
+            // the stream releases its dependents only after its own grid-dependency wait.  Only
+            // the shrink output (read by the epilogue warps) needs this grid's wait.
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
                 const int s = i % stages;
-                if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
+                if (i >= stages && !mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tma_load_2d(smem + s * stage_bytes, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM);
                 tma_load_2d(smem + s * stage_bytes + w_bytes, &tmX, &full[s], (kb0 + i) * BK, 0);
@@ -379,7 +373,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int D = flags[2];
         const int g_begin = use_lsm ? a.dpre : 0;  // with L_sm the pre-staged group is already applied
         if (a.fuse && D > g_begin) {
-            T* Blate = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 16);
+            T* Blate = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128) +
+                       (size_t)per * BM;  // after the y tile
             const size_t late_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(Blate) - smem);
             const int dlate = max(1, static_cast<int>(late_bytes / ((size_t)BM * R * sizeof(T))));
             for (int g0 = g_begin; g0 < D;) {
@@ -421,31 +416,34 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         bool recv = true;
         if (push && cnt > 0 && a.splits > 1) recv = __all_sync(0xffffffffu, mbar_wait(rbar, 0, flags));
-        if (recv && o < h_out) {
-            T* y = static_cast<T*>(a.y);
-            const uint32_t p_addr = smem_u32(own + row);
+        // the owned [cnt tokens][128 features] tile of y is assembled in shared memory (after the
+        // receive buffer) and written with one TMA store; rows/columns outside y are clipped
+        T* Ysm = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128);
+        if (recv) {
             for (int q0 = 0; q0 < cnt; q0 += 4) {
-                float v[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int q = q0 + u;
-                    v[u] = 0.f;
                     if (q < cnt) {
-                        v[u] = own[q * BM + row] + (use_lsm ? L_sm[q * BM + row] : 0.f);
+                        float v = own[q * BM + row] + (use_lsm ? L_sm[q * BM + row] : 0.f);
                         if (push) {
-                            for (int c = 0; c < a.splits - 1; ++c) v[u] += Rcv[((size_t)c * per + q) * BM + row];
+                            for (int c = 0; c < a.splits - 1; ++c) v += Rcv[((size_t)c * per + q) * BM + row];
                         } else {
+                            const uint32_t p_addr = smem_u32(own + q * BM + row);
                             for (int c = 0; c < a.splits; ++c)
-                                if (c != rank)
-                                    v[u] += ld_dsmem_f32(mapa_shared(p_addr + static_cast<uint32_t>(q * BM * 4),
-                                                                     static_cast<uint32_t>(c)));
+                                if (c != rank) v += ld_dsmem_f32(mapa_shared(p_addr, static_cast<uint32_t>(c)));
                         }
+                        Ysm[q * BM + row] = from_f32<T>(v);
                     }
                 }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (q0 + u < cnt) y[(size_t)(t0 + q0 + u) * h_out + o] = from_f32<T>(v[u]);
             }
+            fence_proxy_async_smem();
+        }
+        named_bar_sync(1, 128);
+        if (et == 0 && recv && cnt > 0) {
+            tma_store_2d(&tmY, Ysm, m_tile * BM, t0);
+            bulk_commit_group();
+            bulk_wait_group_read0();
         }
     }
     tc_fence_before();
@@ -697,8 +695,9 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     const size_t limit = 225 * 1024;
     // stage area after the main loop: P [n_pad][128] + receive buffer [splits-1][per][128]
     // (exchange by bulk copies) + one late B tile
-    const size_t park_push = (size_t)p.n_pad * BM * 4 + (size_t)(p.splits - 1) * per * BM * 4 + 16 + slot_b;
-    const size_t park_pull = (size_t)p.n_pad * BM * 4 + 16 + slot_b;
+    const size_t ytile = (size_t)per * BM * 2 + 128;
+    const size_t park_push = (size_t)p.n_pad * BM * 4 + (size_t)(p.splits - 1) * per * BM * 4 + ytile + slot_b;
+    const size_t park_pull = (size_t)p.n_pad * BM * 4 + ytile + slot_b;
     p.push = 1;
     p.stages = 0;
     p.dpre = 0;
@@ -742,10 +741,13 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     const int bf16 = pv.dtype == LORA_BF16;
     if (n <= kDecodeMaxN) {
         const DecodePlan p = plan_decode(pv, n, s_parts);
-        CUtensorMap mW, mX;
+        CUtensorMap mW, mX, mY;
         int rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, BM);
         if (rc) return rc;
         rc = make_map(&mX, x, bf16, pv.h_in, n, p.n_pad);
+        if (rc) return rc;
+        const int per = (p.n_pad + p.splits - 1) / p.splits;
+        rc = make_map_plain(&mY, y, bf16, pv.h_out, n, BM, per);
         if (rc) return rc;
         DecodeArgs a;
         a.pool = pv;
@@ -770,7 +772,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
                                                227 * 1024));
             attr_set = true;
         }
-        void* args[] = {(void*)&mW, (void*)&mX, (void*)&a};
+        void* args[] = {(void*)&mW, (void*)&mX, (void*)&mY, (void*)&a};
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(p.m_tiles, p.splits);

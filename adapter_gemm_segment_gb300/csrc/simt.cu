@@ -81,8 +81,10 @@ template <typename T>
 __global__ void __launch_bounds__(128)
 shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
     __shared__ float red[4][8];
-    pdl_trigger();  // dependents wait for this grid's completion before reading s
+    // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
+    // every kernel before this one has completed (x, W) and waits separately for s.
     pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x, g = blockIdx.y, ks = blockIdx.z;
     const int h = pool.h_in, R = pool.R;
     const int k = ks * kShrKChunk + threadIdx.x * 8;

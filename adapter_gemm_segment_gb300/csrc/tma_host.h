@@ -39,5 +39,23 @@ inline int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t cols, u
     return LORA_OK;
 }
 
+// Row-major [rows, cols] 16-bit matrix, box {box_cols, box_rows}, no swizzle (for stores of
+// row-major shared-memory tiles).
+inline int make_map_plain(CUtensorMap* m, const void* base, int bf16, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                          uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return LORA_OK;
+}
+
 }  // namespace tc
 }  // namespace lora
