@@ -110,6 +110,53 @@ __device__ __forceinline__ float lora_dot_smem(const uint4* __restrict__ br, con
     return acc;
 }
 
+// LoRA term of one feature (B row `row`) for up to 8 tokens q0..q0+7 at once, all operands in
+// shared memory; every load of the batch is issued before it is used.  Tokens whose slot index
+// (dloc - g0) is outside [0, Dg) get 0.
+template <typename T>
+__device__ __forceinline__ void lora_batch8(const T* __restrict__ Bg, const float* __restrict__ S_sm,
+                                            const int* __restrict__ dloc_sm, int q0, int cnt, int g0, int Dg, int row,
+                                            int R, int lane, float (&acc)[8]) {
+    const int chunks = R / 8;
+    int d[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        d[u] = q0 + u < cnt ? dloc_sm[q0 + u] - g0 : -1;
+        if (d[u] >= Dg) d[u] = -1;
+        acc[u] = 0.f;
+    }
+    if (Dg <= 0) return;  // nothing staged: do not touch the (empty) B region
+    const uint4* B4 = reinterpret_cast<const uint4*>(Bg);
+    for (int jj = 0; jj < chunks; ++jj) {
+        const int jc = (jj + lane) % chunks;  // staggered: conflict-free rows for any r_max
+        uint4 bv[8];
+        float4 s0[8], s1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int du = d[u] < 0 ? 0 : d[u];
+            bv[u] = B4[(size_t)(du * BM + row) * chunks + jc];
+            const float4* sp = reinterpret_cast<const float4*>(S_sm + min(q0 + u, cnt - 1) * R + jc * 8);
+            s0[u] = sp[0];
+            s1[u] = sp[1];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float b[8];
+            unpack8<T>(bv[u], b);
+            float v = acc[u];
+            v = fmaf(b[0], s0[u].x, v);
+            v = fmaf(b[1], s0[u].y, v);
+            v = fmaf(b[2], s0[u].z, v);
+            v = fmaf(b[3], s0[u].w, v);
+            v = fmaf(b[4], s1[u].x, v);
+            v = fmaf(b[5], s1[u].y, v);
+            v = fmaf(b[6], s1[u].z, v);
+            v = fmaf(b[7], s1[u].w, v);
+            acc[u] = d[u] >= 0 ? v : 0.f;
+        }
+    }
+}
+
 // ============================================================================================
 // decode: swap-AB + split-K over a thread-block cluster
 // ============================================================================================
@@ -313,13 +360,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             named_bar_sync(1, 128);
             // LoRA term of this thread's feature for every owned token whose slot is pre-staged
             if (use_lsm) {
-                for (int q = 0; q < cnt; ++q) {
-                    const int d = dloc_sm[q];
-                    float acc = 0.f;
-                    if (staged && d >= 0 && d < Dg)
-                        acc = lora_dot_smem<T>(reinterpret_cast<const uint4*>(Bpre) + (size_t)(d * BM + row) * chunks,
-                                               S_sm + q * R, chunks, lane);
-                    L_sm[q * BM + row] = acc;
+                for (int q0 = 0; q0 < cnt; q0 += 8) {
+                    float acc[8];
+                    lora_batch8<T>(Bpre, S_sm, dloc_sm, q0, cnt, 0, staged ? Dg : 0, row, R, lane, acc);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (q0 + u < cnt) L_sm[(q0 + u) * BM + row] = acc[u];
                 }
             }
         } else if (use_lsm) {
@@ -405,11 +451,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     }
                     named_bar_sync(1, 128);
                 }
-                for (int q = 0; q < cnt; ++q) {
-                    const int d = dloc_sm[q] - g0;
-                    if (d < 0 || d >= Dg) continue;
-                    own[q * BM + row] += lora_dot_smem<T>(reinterpret_cast<const uint4*>(Bg) + (size_t)(d * BM + row) * chunks,
-                                                          S_sm + q * R, chunks, lane);
+                for (int q0 = 0; q0 < cnt; q0 += 8) {
+                    float acc[8];
+                    lora_batch8<T>(Bg, S_sm, dloc_sm, q0, cnt, g0, Dg, row, R, lane, acc);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (q0 + u < cnt) own[(q0 + u) * BM + row] += acc[u];
                 }
                 g0 += Dg;
             }
@@ -420,22 +467,40 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // receive buffer) and written with one TMA store; rows/columns outside y are clipped
         T* Ysm = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128);
         if (recv) {
-            for (int q0 = 0; q0 < cnt; q0 += 4) {
+            for (int q0 = 0; q0 < cnt; q0 += 8) {  // 8 tokens per batch, every load in flight first
+                float v[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int q = q0 + u;
-                    if (q < cnt) {
-                        float v = own[q * BM + row] + (use_lsm ? L_sm[q * BM + row] : 0.f);
-                        if (push) {
-                            for (int c = 0; c < a.splits - 1; ++c) v += Rcv[((size_t)c * per + q) * BM + row];
-                        } else {
-                            const uint32_t p_addr = smem_u32(own + q * BM + row);
-                            for (int c = 0; c < a.splits; ++c)
-                                if (c != rank) v += ld_dsmem_f32(mapa_shared(p_addr, static_cast<uint32_t>(c)));
+                for (int u = 0; u < 8; ++u) {
+                    const int q = min(q0 + u, cnt - 1);
+                    v[u] = own[q * BM + row];
+                    if (use_lsm) v[u] += L_sm[q * BM + row];
+                }
+                if (push) {
+#pragma unroll
+                    for (int c = 0; c < 7; ++c) {
+                        if (c < a.splits - 1) {
+                            float r8[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) r8[u] = Rcv[((size_t)c * per + min(q0 + u, cnt - 1)) * BM + row];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) v[u] += r8[u];
                         }
-                        Ysm[q * BM + row] = from_f32<T>(v);
+                    }
+                } else {
+                    for (int c = 0; c < a.splits; ++c) {
+                        if (c == rank) continue;
+                        float r8[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            r8[u] = ld_dsmem_f32(mapa_shared(smem_u32(own + min(q0 + u, cnt - 1) * BM + row),
+                                                             static_cast<uint32_t>(c)));
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) v[u] += r8[u];
                     }
                 }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (q0 + u < cnt) Ysm[(q0 + u) * BM + row] = from_f32<T>(v[u]);
             }
             fence_proxy_async_smem();
         }
