@@ -33,7 +33,7 @@ EXPORTED = (
     "lora_pool_bytes", "lora_pool_create", "lora_pool_destroy", "lora_pool_load_slot", "lora_pool_unload_slot",
     "lora_segment_workspace_bytes", "lora_segment", "lora_segment_status", "lora_linear_workspace_bytes",
     "lora_linear_fwd", "lora_linear_policy", "lora_last_error", "lora_kernel_launch_count",
-    "lora_set_timing_events",
+    "lora_set_timing_events", "lora_linear_fwd_static_ws",
 )
 
 
@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "lora_linear_fwd": [vp, vp, vp, vp, P(lora_segments), i32, vp, sz, vp],
         "lora_linear_policy": [vp, i32, P(i32)],
         "lora_set_timing_events": [vp, vp, vp],
+        "lora_linear_fwd_static_ws": [vp, vp, vp, vp, P(lora_segments), i32, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -187,6 +188,16 @@ def lora_linear_workspace_bytes(pool_handle, n_tokens: int) -> int:
     out = ctypes.c_size_t()
     _check(_lib.lora_linear_workspace_bytes(pool_handle, n_tokens, ctypes.byref(out)))
     return out.value
+
+
+def lora_linear_fwd_static_ws(pool_handle, W: torch.Tensor, x: torch.Tensor, y: torch.Tensor, seg: lora_segments,
+                              variant: int = LORA_VARIANT_AUTO, stream=None) -> torch.Tensor:
+    """lora_linear_fwd for callers that cannot provide a workspace: the library's own fixed
+    4 MiB device array holds the shrink output.  Calls that may overlap on the GPU share it
+    and race; the first call on a device must come before any stream capture."""
+    _check(_lib.lora_linear_fwd_static_ws(pool_handle, _ptr(_dev(W, "W")), _ptr(_dev(x, "x")), _ptr(_dev(y, "y")),
+                                          ctypes.byref(seg), variant, _stream(stream)))
+    return y
 
 
 def lora_linear_policy(pool_handle, n_tokens: int) -> int:

@@ -1,0 +1,100 @@
+// lora_linear_fwd_static_ws: the LoRA-augmented linear for callers that cannot give the library
+// a workspace.
+//
+// Some hosts cannot allocate device memory when they call into this library.  One example is
+// a plugin or operator that runs inside someone else's engine, which hands it only its
+// inputs and outputs.  Another is code that enqueues work while a CUDA graph is being
+// captured, or under a fixed memory budget that does not allow growth.  In those settings
+// cudaMalloc is not an option: it synchronises the device, it is not allowed during stream
+// capture, and it may be forbidden by the host.
+//
+// For them, the shrink output that lora_linear_fwd keeps in the caller's workspace lives here
+// in a fixed device array that belongs to the library.  Every GPU that loads the library
+// holds kStaticWsBytes of it until the process exits.
+//
+// The first call on a device looks up the array's device address with
+// cudaGetSymbolAddress and caches it; make that first call before any stream capture.  All
+// calls share the one array: calls that may run at the same time on the GPU (different
+// streams, or graphs replayed concurrently) overwrite each other's data.  Nothing in the
+// array has to start at zero -- every value a call reads was written earlier in the same call.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+namespace {
+
+constexpr size_t kStaticWsBytes = size_t(4) << 20;  // 4 MiB of float32 shrink output
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+std::mutex g_static_ws_mu;
+void* g_static_ws_ptr[kMaxDevices] = {};
+
+// Device address of g_static_ws on the current device (looked up once per device).
+int static_ws_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(LORA_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return set_error(LORA_EUNSUP, "device ordinal %d >= %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_static_ws_mu);
+    if (!g_static_ws_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_ws);
+        if (e != cudaSuccess || !p)
+            return set_error(LORA_ECUDA, "cudaGetSymbolAddress(static workspace): %s", cudaGetErrorString(e));
+        g_static_ws_ptr[dev] = p;
+    }
+    *out = g_static_ws_ptr[dev];
+    return LORA_OK;
+}
+
+}  // namespace
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" int lora_linear_fwd_static_ws(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
+                                         const lora_segments* seg, int variant, void* stream) {
+    if (!pool || !seg) return set_error(LORA_EINVAL, "pool/seg is NULL");
+    const PoolView pv = pool_view(pool);
+    const int n = seg->n_tokens;
+    if (seg->n_slots != pv.S)
+        return set_error(LORA_EINVAL, "segments were built for %d slots, pool has %d", seg->n_slots, pv.S);
+    if (variant < LORA_VARIANT_AUTO || variant > LORA_VARIANT_CUDA_CORE)
+        return set_error(LORA_EINVAL, "bad variant %d", variant);
+    if (n == 0) return LORA_OK;
+    if (!W_dev || !x_dev || !y_dev) return set_error(LORA_EINVAL, "W/x/y is NULL");
+    const size_t align = pv.dtype != LORA_F32 ? 16 : 4;
+    if ((reinterpret_cast<uintptr_t>(W_dev) | reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(y_dev)) %
+        align)
+        return set_error(LORA_EINVAL, "W/x/y must be %zu-byte aligned", align);
+    const size_t need = sizeof(float) * (size_t)n * pv.R * (size_t)shrink_parts(pv, n, false);
+    if (need > kStaticWsBytes)
+        return set_error(LORA_ENOSPACE,
+                         "static workspace holds %zu bytes, this call needs %zu (n=%d, r_max=%d): use lora_linear_fwd "
+                         "with a caller workspace",
+                         kStaticWsBytes, need, n, pv.R);
+    void* ws = nullptr;
+    int rc = static_ws_address(&ws);
+    if (rc) return rc;
+    float* s_buf = static_cast<float*>(ws);
+    if (variant == LORA_VARIANT_AUTO) lora_linear_policy(pool, n, &variant);
+    const SegView sv = seg_view(seg);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool tc = variant != LORA_VARIANT_CUDA_CORE && tc_supported(pv, n);
+    const bool fused = variant != LORA_VARIANT_SEPARATE;
+    int s_parts = 1;
+    if (tc && n > 256 && shrink_tc_supported(pv))
+        rc = launch_shrink_tc(pv, sv, x_dev, s_buf, st);
+    else
+        rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256, &s_parts);
+    if (rc) return rc;
+    rc = tc ? launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st)
+            : launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
+    if (rc) return rc;
+    if (!fused) return launch_expand(pv, sv, s_buf, s_parts, y_dev, st);
+    return LORA_OK;
+}

@@ -171,6 +171,20 @@ int lora_linear_workspace_bytes(lora_pool_t pool, int n_tokens, size_t* bytes);
 int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
                     const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes, void* stream);
 
+/* lora_linear_fwd without a caller workspace (the multi-LoRA pages have no counterpart; this
+ * is a convenience of this library).  For hosts that cannot allocate device memory when they
+ * call in -- for example a plugin inside another engine that is handed only its inputs and
+ * outputs, or code enqueueing during CUDA graph capture, where cudaMalloc is not allowed.
+ * Arguments and results are those of lora_linear_fwd; the shrink output goes to a fixed
+ * 4 MiB device array owned by the library (held on every GPU that loads the library until the
+ * process exits), so calls that need more (4 * n * r_max * ceil(h_in/1024) bytes for batches
+ * of up to 256 tokens, 4 * n * r_max above) fail with LORA_ENOSPACE.  This function allocates
+ * nothing.  Its first call on a device looks up the array's address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  All calls share the array, so calls that
+ * can overlap on the GPU (several streams, concurrent graph replays) race with each other. */
+int lora_linear_fwd_static_ws(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
+                              const lora_segments* seg, int variant, void* stream);
+
 /* Which variant LORA_VARIANT_AUTO picks for n_tokens on this pool (1 or 2). */
 int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant);
 
