@@ -33,7 +33,7 @@ EXPORTED = (
     "lora_pool_bytes", "lora_pool_create", "lora_pool_destroy", "lora_pool_load_slot", "lora_pool_unload_slot",
     "lora_segment_workspace_bytes", "lora_segment", "lora_segment_status", "lora_linear_workspace_bytes",
     "lora_linear_fwd", "lora_linear_policy", "lora_last_error", "lora_kernel_launch_count",
-    "lora_set_timing_events", "lora_linear_fwd_static_ws",
+    "lora_set_timing_events", "lora_linear_fwd_static_ws", "lora_linear_fwd_ex",
 )
 
 
@@ -75,6 +75,7 @@ def _load() -> ctypes.CDLL:
         "lora_linear_policy": [vp, i32, P(i32)],
         "lora_set_timing_events": [vp, vp, vp],
         "lora_linear_fwd_static_ws": [vp, vp, vp, vp, P(lora_segments), i32, vp],
+        "lora_linear_fwd_ex": [vp, vp, vp, vp, P(lora_segments), i32, vp, sz, vp, sz, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -188,6 +189,19 @@ def lora_linear_workspace_bytes(pool_handle, n_tokens: int) -> int:
     out = ctypes.c_size_t()
     _check(_lib.lora_linear_workspace_bytes(pool_handle, n_tokens, ctypes.byref(out)))
     return out.value
+
+
+def lora_linear_fwd_ex(pool_handle, W: torch.Tensor, x: torch.Tensor, y: torch.Tensor, seg: lora_segments,
+                       ws: torch.Tensor, variant: int = LORA_VARIANT_AUTO, prefetch: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """lora_linear_fwd with an L2 prefetch hint: `prefetch` (e.g. the next linear's weight) is
+    streamed into L2 while this call's epilogue runs.  Results are identical without it."""
+    pf = _ptr(_dev(prefetch, "prefetch")) if prefetch is not None else ctypes.c_void_p(0)
+    pf_bytes = prefetch.numel() * prefetch.element_size() if prefetch is not None else 0
+    _check(_lib.lora_linear_fwd_ex(pool_handle, _ptr(_dev(W, "W")), _ptr(_dev(x, "x")), _ptr(_dev(y, "y")),
+                                   ctypes.byref(seg), variant, _ptr(_dev(ws, "ws")), ws.numel() * ws.element_size(),
+                                   pf, pf_bytes, _stream(stream)))
+    return y
 
 
 def lora_linear_fwd_static_ws(pool_handle, W: torch.Tensor, x: torch.Tensor, y: torch.Tensor, seg: lora_segments,

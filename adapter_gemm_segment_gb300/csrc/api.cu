@@ -120,6 +120,12 @@ int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant) {
 
 int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev, const lora_segments* seg,
                     int variant, void* ws_dev, size_t ws_bytes, void* stream) {
+    return lora_linear_fwd_ex(pool, W_dev, x_dev, y_dev, seg, variant, ws_dev, ws_bytes, nullptr, 0, stream);
+}
+
+int lora_linear_fwd_ex(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev, const lora_segments* seg,
+                       int variant, void* ws_dev, size_t ws_bytes, const void* prefetch_dev, size_t prefetch_bytes,
+                       void* stream) {
     if (!pool || !seg) return set_error(LORA_EINVAL, "pool/seg is NULL");
     const PoolView pv = pool_view(pool);
     const int n = seg->n_tokens;
@@ -128,6 +134,8 @@ int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void
     if (variant < LORA_VARIANT_AUTO || variant > kVariantCudaCore) return set_error(LORA_EINVAL, "bad variant %d", variant);
     if (n == 0) return LORA_OK;
     if (!W_dev || !x_dev || !y_dev || !ws_dev) return set_error(LORA_EINVAL, "W/x/y/ws is NULL");
+    if (prefetch_dev && (reinterpret_cast<uintptr_t>(prefetch_dev) % 16))
+        return set_error(LORA_EINVAL, "prefetch range must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(ws_dev) % 256) return set_error(LORA_EINVAL, "ws must be 256-byte aligned");
     if (pv.dtype != LORA_F32) {
         if ((reinterpret_cast<uintptr_t>(W_dev) | reinterpret_cast<uintptr_t>(x_dev) |
@@ -157,7 +165,7 @@ int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void
     if (rc) return rc;
     record_if(g_ev_before_gemm, st);
     if (tc) {
-        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
+        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st, prefetch_dev, prefetch_bytes);
     } else {
         rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
     }

@@ -54,6 +54,8 @@ struct DecodeArgs {
     int s_parts;  // K-parts of the shrink output to sum
     int dpre;     // distinct slots whose B rows are staged during the main loop
     int push;     // exchange partials by bulk copies (1) or remote loads (0)
+    const char* prefetch;  // optional range streamed into L2 once this CTA's loads are issued
+    size_t prefetch_bytes;
 };
 
 struct PrefillArgs {
@@ -267,6 +269,17 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - tw < kWaitLimitNs) {
                     }
                 }
+            } else if (a.prefetch && a.prefetch_bytes) {
+                // HBM would idle through the epilogue: stream this CTA's slice of the caller's
+                // prefetch range (typically the next linear's weight) into L2 meanwhile.
+                const size_t ncta = (size_t)gridDim.x * gridDim.y;
+                const size_t cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+                const size_t slice = ((a.prefetch_bytes + ncta - 1) / ncta + 15) & ~size_t(15);
+                const size_t beg = cta * slice;
+                const size_t cap = a.prefetch_bytes & ~size_t(15);
+                const size_t end = cap < beg + slice ? cap : beg + slice;
+                for (size_t off = beg; off < end; off += 65536)
+                    prefetch_l2_bulk(a.prefetch + off, static_cast<uint32_t>(end - off < 65536 ? end - off : 65536));
             }
         }
     } else if (warp == 1) {
@@ -799,7 +812,7 @@ int tc_supported(const PoolView& pv, int n) {
 
 template <typename T>
 static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
-                       int s_parts, void* y, bool fuse, cudaStream_t st) {
+                       int s_parts, void* y, bool fuse, const void* prefetch, size_t prefetch_bytes, cudaStream_t st) {
     using namespace tc;
     const int n = sv.n;
     if (n == 0) return LORA_OK;
@@ -831,6 +844,8 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.s_parts = s_parts;
         a.dpre = p.dpre;
         a.push = p.push;
+        a.prefetch = static_cast<const char*>(prefetch);
+        a.prefetch_bytes = prefetch ? prefetch_bytes : 0;
         static bool attr_set = false;
         if (!attr_set) {
             LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -892,9 +907,10 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
 }
 
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
-                   void* y, bool fuse, cudaStream_t st) {
-    if (pv.dtype == LORA_F16) return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, st);
-    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, st);
+                   void* y, bool fuse, cudaStream_t st, const void* prefetch, size_t prefetch_bytes) {
+    if (pv.dtype == LORA_F16)
+        return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, st);
+    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, st);
 }
 
 }  // namespace lora

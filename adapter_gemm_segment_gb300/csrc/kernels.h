@@ -27,8 +27,10 @@ int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const
 //                 of a thread-block cluster, reduced through distributed shared memory.
 //   prefill path (n > 256):  token tiles on M (128), outputs on N (256), persistent CTAs.
 int tc_supported(const PoolView& pv, int n);
+// prefetch/prefetch_bytes: optional device range the decode kernel streams into L2 after its
+// own loads (ignored by the prefill kernel).
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
-                   void* y, bool fuse, cudaStream_t st);
+                   void* y, bool fuse, cudaStream_t st, const void* prefetch = nullptr, size_t prefetch_bytes = 0);
 
 // Grouped tcgen05 shrink for batches of more than 256 tokens (one CTA per 128-token tile).
 int shrink_tc_supported(const PoolView& pv);

@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the cpu_baseline leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-prefetch-next", action="store_true",
+                   help="do not pass the next linear's weight as the L2 prefetch hint")
     a = p.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload]
@@ -346,10 +348,16 @@ def ours(args):
 
     launches_before = ags.lora_kernel_launch_count()
 
+    prefetch = not args.no_prefetch_next and args.workload != "prefill"
+    nxt = [layers[(i + 1) % len(layers)]["W"] if prefetch else None for i in range(len(layers))]
+
+    def linear(i, L, seg):
+        ags.lora_linear_fwd_ex(L["pool"].handle, L["W"], L["x"], L["y"], seg, lin_ws, args.variant, prefetch=nxt[i])
+
     def step():
         seg = ags.lora_segment(idx_dev, pool0.handle, seg_ws)
-        for L in layers:
-            ags.lora_linear_fwd(L["pool"].handle, L["W"], L["x"], L["y"], seg, lin_ws, args.variant)
+        for i, L in enumerate(layers):
+            linear(i, L, seg)
 
     # eager warm-up (also checks the status word once)
     step()
@@ -410,9 +418,9 @@ def ours(args):
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
         seg = ags.lora_segment(idx_dev, pool0.handle, seg_ws)
-        for L, trio in zip(layers, evs):
+        for i, (L, trio) in enumerate(zip(layers, evs)):
             ags.lora_set_timing_events(*trio)
-            ags.lora_linear_fwd(L["pool"].handle, L["W"], L["x"], L["y"], seg, lin_ws, args.variant)
+            linear(i, L, seg)
         ags.lora_set_timing_events()
     reps = max(3, min(50, args.steps // 20))
     g2.replay()
@@ -501,6 +509,7 @@ def ours(args):
                     "policy_variant": ags.lora_linear_policy(pool0.handle, n),
                     "distinct_slots_touched": alg["D"], "lora_tokens": alg["n_L"],
                     "l2": "inputs larger than L2 (no flush)", "timing": "CUDA graph replay, CUDA events",
+                    "l2_prefetch_next_weight": prefetch,
                     "parallelism": f"replicas x{world} (token batches sharded across GPUs, no collective)"})
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

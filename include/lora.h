@@ -171,6 +171,17 @@ int lora_linear_workspace_bytes(lora_pool_t pool, int n_tokens, size_t* bytes);
 int lora_linear_fwd(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
                     const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes, void* stream);
 
+/* lora_linear_fwd plus an L2 prefetch hint (GB300 has a 129 MB L2, larger than one base
+ * weight).  prefetch_dev / prefetch_bytes: an optional device range, 16-byte aligned --
+ * typically the base weight of the next linear the caller will run on this stream.  Once a
+ * decode-path CTA (n <= 256 tokens) has issued its own loads, it streams its share of that
+ * range into L2 while its epilogue runs, so the next linear finds most of its weight in L2.
+ * Purely a hint: results are identical with or without it; the range is only read.  NULL
+ * (or 0 bytes) means no prefetch, which is exactly lora_linear_fwd. */
+int lora_linear_fwd_ex(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
+                       const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes,
+                       const void* prefetch_dev, size_t prefetch_bytes, void* stream);
+
 /* lora_linear_fwd without a caller workspace (the multi-LoRA pages have no counterpart; this
  * is a convenience of this library).  For hosts that cannot allocate device memory when they
  * call in -- for example a plugin inside another engine that is handed only its inputs and

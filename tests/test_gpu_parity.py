@@ -218,6 +218,22 @@ def test_small_cases(lib, spec, variant):
                                               case.idx.numpy()), f"{case.name} W=0 variant {variant}")
 
 
+def test_l2_prefetch_hint_does_not_change_results(lib):
+    case = wl.decode_q_proj(n=32, h=1024)
+    pool = make_pool(lib, case)
+    seg = pool.segment(case.idx.to(DEV))
+    W, x = case.W.to(DEV), case.x.to(DEV)
+    ws = pool.linear_workspace(case.n)
+    W_next = torch.randn(1024, 1024, device=DEV).half()
+    y0 = torch.empty(case.n, case.h_out, dtype=case.dtype, device=DEV)
+    y1 = torch.empty_like(y0)
+    lib.lora_linear_fwd(pool.handle, W, x, y0, seg, ws, 1)
+    lib.lora_linear_fwd_ex(pool.handle, W, x, y1, seg, ws, 1, prefetch=W_next)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    assert_parity(y1.cpu(), O.lora_linear_case(case), "prefetch hint")
+
+
 def test_repeated_calls_are_bit_identical(lib):
     case = wl.decode_q_proj(n=48, h=1024)
     pool = make_pool(lib, case)
