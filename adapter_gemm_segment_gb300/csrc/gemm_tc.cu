@@ -54,7 +54,7 @@ struct DecodeArgs {
     int s_parts;  // K-parts of the shrink output to sum
     int dpre;     // distinct slots whose B rows are staged during the main loop
     int push;     // exchange partials by bulk copies (1) or remote loads (0)
-    const char* prefetch;  // optional range streamed into L2 once this CTA's loads are issued
+    const char* prefetch;  // optional range streamed into L2 once this CTA's accumulator is complete
     size_t prefetch_bytes;
 };
 
@@ -216,7 +216,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     float* Rcv = P + (size_t)a.n_pad * BM;
     const bool push = a.push != 0;
 
+    const int pre = min(stages, nkb);  // first ring pass, issued before the block-wide sync
     if (threadIdx.x == 0) {
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -226,10 +229,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         mbar_init(rbar, 1);
         for (int i = 0; i < 8; ++i) flags[i] = 0;
         fence_barrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmW);
-        prefetch_tmap(&tmX);
+        // W and x are complete when this grid starts (see the producer below)
+        for (int i = 0; i < pre; ++i) {
+            mbar_arrive_expect_tx(&full[i], stage_bytes);
+            tma_load_2d(smem + i * stage_bytes, &tmW, &full[i], (kb0 + i) * BK, m_tile * BM);
+            tma_load_2d(smem + i * stage_bytes + w_bytes, &tmX, &full[i], (kb0 + i) * BK, 0);
+        }
         prefetch_tmap(&tmY);
     }
     if (warp == 1) {
@@ -253,10 +258,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // W and x are complete when this grid starts: the shrink kernel that precedes it in
             // the stream releases its dependents only after its own grid-dependency wait.  Only
             // the shrink output (read by the epilogue warps) needs this grid's wait.
-            int issued = 0;
-            for (int i = 0; i < nkb; ++i) {
+            int issued = pre;
+            for (int i = pre; i < nkb; ++i) {
                 const int s = i % stages;
-                if (i >= stages && !mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
+                if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tma_load_2d(smem + s * stage_bytes, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM);
                 tma_load_2d(smem + s * stage_bytes + w_bytes, &tmX, &full[s], (kb0 + i) * BK, 0);
@@ -269,17 +274,6 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - tw < kWaitLimitNs) {
                     }
                 }
-            } else if (a.prefetch && a.prefetch_bytes) {
-                // HBM would idle through the epilogue: stream this CTA's slice of the caller's
-                // prefetch range (typically the next linear's weight) into L2 meanwhile.
-                const size_t ncta = (size_t)gridDim.x * gridDim.y;
-                const size_t cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
-                const size_t slice = ((a.prefetch_bytes + ncta - 1) / ncta + 15) & ~size_t(15);
-                const size_t beg = cta * slice;
-                const size_t cap = a.prefetch_bytes & ~size_t(15);
-                const size_t end = cap < beg + slice ? cap : beg + slice;
-                for (size_t off = beg; off < end; off += 65536)
-                    prefetch_l2_bulk(a.prefetch + off, static_cast<uint32_t>(end - off < 65536 ? end - off : 65536));
             }
         }
     } else if (warp == 1) {
@@ -387,6 +381,19 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // ---- phase B: park the partial tile in the idle stages ----
         const bool got = mbar_wait(tmem_full, 0, flags);
         tc_fence_after();
+        if (et == 0 && got && a.prefetch && a.prefetch_bytes) {
+            // This CTA's share of W has been consumed and HBM would idle through the epilogue:
+            // stream this CTA's slice of the caller's prefetch range (typically the next
+            // linear's weight) into L2 meanwhile.
+            const size_t ncta = (size_t)gridDim.x * gridDim.y;
+            const size_t cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+            const size_t slice = ((a.prefetch_bytes + ncta - 1) / ncta + 15) & ~size_t(15);
+            const size_t beg = cta * slice;
+            const size_t cap = a.prefetch_bytes & ~size_t(15);
+            const size_t end = cap < beg + slice ? cap : beg + slice;
+            for (size_t off = beg; off < end; off += 65536)
+                prefetch_l2_bulk(a.prefetch + off, static_cast<uint32_t>(end - off < 65536 ? end - off : 65536));
+        }
         named_bar_sync(1, 128);
         if (et == 0) {
             flags[1] = (got && !flags[0] && flags[3] == LORA_OK) ? 1 : 0;

@@ -55,8 +55,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the cpu_baseline leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--no-prefetch-next", action="store_true",
-                   help="do not pass the next linear's weight as the L2 prefetch hint")
+    p.add_argument("--prefetch-next", action="store_true",
+                   help="pass the next linear's weight as the L2 prefetch hint of lora_linear_fwd_ex")
     a = p.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload]
@@ -348,7 +348,7 @@ def ours(args):
 
     launches_before = ags.lora_kernel_launch_count()
 
-    prefetch = not args.no_prefetch_next and args.workload != "prefill"
+    prefetch = args.prefetch_next and args.workload != "prefill"
     nxt = [layers[(i + 1) % len(layers)]["W"] if prefetch else None for i in range(len(layers))]
 
     def linear(i, L, seg):
