@@ -216,10 +216,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     float* Rcv = P + (size_t)a.n_pad * BM;
     const bool push = a.push != 0;
 
-    const int pre = min(stages, nkb);  // first ring pass, issued before the block-wide sync
     if (threadIdx.x == 0) {
-        prefetch_tmap(&tmW);
-        prefetch_tmap(&tmX);
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -229,12 +226,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         mbar_init(rbar, 1);
         for (int i = 0; i < 8; ++i) flags[i] = 0;
         fence_barrier_init();
-        // W and x are complete when this grid starts (see the producer below)
-        for (int i = 0; i < pre; ++i) {
-            mbar_arrive_expect_tx(&full[i], stage_bytes);
-            tma_load_2d(smem + i * stage_bytes, &tmW, &full[i], (kb0 + i) * BK, m_tile * BM);
-            tma_load_2d(smem + i * stage_bytes + w_bytes, &tmX, &full[i], (kb0 + i) * BK, 0);
-        }
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
         prefetch_tmap(&tmY);
     }
     if (warp == 1) {
@@ -258,10 +253,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // W and x are complete when this grid starts: the shrink kernel that precedes it in
             // the stream releases its dependents only after its own grid-dependency wait.  Only
             // the shrink output (read by the epilogue warps) needs this grid's wait.
-            int issued = pre;
-            for (int i = pre; i < nkb; ++i) {
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
                 const int s = i % stages;
-                if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
+                if (i >= stages && !mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tma_load_2d(smem + s * stage_bytes, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM);
                 tma_load_2d(smem + s * stage_bytes + w_bytes, &tmX, &full[s], (kb0 + i) * BK, 0);
