@@ -39,7 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "LoRA-linear tokens/s at 1 GB300 + % of HBM (decode) / tensor (prefill) roofline"
 UNIT = "tokens/s"
-DEFAULT_STEPS = {"decode": 4000, "mixed": 4000, "prefill": 400}
+DEFAULT_STEPS = {"decode": 4000, "mixed": 4000, "prefill": 400, "layer": 1000}
 
 
 def parse_args():
@@ -48,9 +48,9 @@ def parse_args():
     p.add_argument("--steps", type=int, default=None)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["decode", "prefill", "mixed"], default="decode")
+    p.add_argument("--workload", choices=["decode", "prefill", "mixed", "layer"], default="decode")
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 fused, 2 separate, 3 CUDA-core")
-    p.add_argument("--layers", type=int, default=32)
+    p.add_argument("--layers", type=int, default=None, help="layer copies per step (32; 4 for --workload layer)")
     p.add_argument("--tokens", type=int, default=64, help="batch size of the decode/mixed workloads")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the cpu_baseline leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -60,6 +60,8 @@ def parse_args():
     a = p.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload]
+    if a.layers is None:
+        a.layers = 4 if a.workload == "layer" else 32
     a.warmup = max(3, a.warmup)
     return a
 
@@ -86,7 +88,7 @@ def workload_cases(name, rank, layers, tokens, layer_range=None):
 
     layer_range = range(layers) if layer_range is None else layer_range
     if name == "decode":
-        seed = 1 + 100 * rank
+        seed = 1 + rank_seed_offset(rank)
         first = wl.decode_q_proj(seed=seed, n=tokens, layer=0)
         cases = [first if l == 0 else wl.decode_q_proj(seed=seed, n=tokens, layer=l) for l in layer_range]
         desc = {"workload": f"decode q_proj 4096x4096 fp16, {tokens} tokens, {layers} layers per step, "
@@ -95,7 +97,7 @@ def workload_cases(name, rank, layers, tokens, layer_range=None):
                 "n_slots": 100}
         return first.idx, cases, desc
     if name == "mixed":
-        seed = 2 + 100 * rank
+        seed = 2 + rank_seed_offset(rank)
         first = wl.mixed_rank(tokens, seed=seed, layer=0)
         cases = [first if l == 0 else wl.mixed_rank(tokens, seed=seed, layer=l) for l in layer_range]
         desc = {"workload": f"mixed-rank decode 4096x4096 fp16, {tokens} tokens, {layers} layers per step, "
@@ -103,31 +105,71 @@ def workload_cases(name, rank, layers, tokens, layer_range=None):
                 "tokens": tokens, "linears_per_step": layers, "h_in": 4096, "h_out": 4096, "r_max": 64,
                 "n_slots": 6}
         return first.idx, cases, desc
-    cases = wl.prefill(seed=3 + 100 * rank)
+    if name == "layer":
+        cases = []
+        for l in layer_range:
+            cases += wl.full_layer(l, seed=4 + rank_seed_offset(rank))
+        desc = {"workload": f"7B-shaped decode layers: 256 tokens bf16 through q,k,v,o (4096x4096), gate/up "
+                            f"(4096x11008), down (11008x4096) of {layers} layers per step, LoRA r=16 alpha=32 on "
+                            "all seven, 100 adapters each, Zipf(1.1)",
+                "tokens": 256, "linears_per_step": 7 * layers, "r_max": 16, "n_slots": 100}
+        return (cases[0].idx if cases else _layer_idx(rank)), cases, desc
+    cases = wl.prefill(seed=3 + rank_seed_offset(rank))
     desc = {"workload": "prefill 32x512 tokens bf16, q_proj + v_proj 4096x4096, 100 adapters r=16 alpha=32",
             "tokens": 16384, "linears_per_step": 2, "h_in": 4096, "h_out": 4096, "r_max": 16, "n_slots": 100}
     return cases[0].idx, cases, desc
 
 
-def algorithmic(case_like, idx, desc):
-    """Per-linear algorithmic bytes / FLOPs (W + touched adapters + x + y; base + LoRA)."""
+def _layer_idx(rank):
+    import numpy as np
+    import torch
+
+    from adapter_gemm_segment_gb300 import workloads as wl
+
+    rng = np.random.default_rng([4 + rank_seed_offset(rank)])
+    return torch.from_numpy(wl.draw_zipf_idx(rng, 256, 100))
+
+
+def algorithmic_case(idx, h_in, h_out, R, es=2):
+    """One linear's algorithmic bytes / FLOPs (W + touched adapters + x + y; base + LoRA)."""
     import numpy as np
 
     idx = np.asarray(idx)
-    n, h_in, h_out, R = len(idx), desc["h_in"], desc["h_out"], desc["r_max"]
-    es = 2
+    n = len(idx)
     D = len(set(idx[idx >= 0].tolist()))
     n_L = int((idx >= 0).sum())
     W = h_out * h_in * es
     A_D = D * R * h_in * es
     B_D = D * h_out * R * es
     xy = n * (h_in + h_out) * es
-    return {"D": D, "n_L": n_L,
-            "linear_bytes": W + A_D + B_D + xy,
-            "gemm_bytes": W + B_D + xy,
+    return {"D": D, "n_L": n_L, "linear_bytes": W + A_D + B_D + xy, "gemm_bytes": W + B_D + xy,
             "linear_flops": 2 * n * h_in * h_out + 2 * n_L * R * (h_in + h_out),
-            "gemm_flops": 2 * n * h_in * h_out + 2 * n_L * R * h_out,
-            "padded_rank_share": None}
+            "gemm_flops": 2 * n * h_in * h_out + 2 * n_L * R * h_out}
+
+
+# ----------------------------------------------------------------------------------------------
+# multi-rank helpers (replicas: every rank runs its own batches; no data-path collective)
+# ----------------------------------------------------------------------------------------------
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest per-rank timing (the job is as slow as its slowest replica)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return world * tokens_per_step * steps / (ms_max / 1e3)
+
+
+def rank_seed_offset(rank: int) -> int:
+    """Each replica draws its own batches (weak scaling: fixed work per GPU)."""
+    return 100 * rank
 
 
 # ----------------------------------------------------------------------------------------------
@@ -396,17 +438,13 @@ def ours(args):
     torch.cuda.synchronize()
     barrier()
     t_host1 = time.time()
-    ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     time.sleep(0.25)
     clocks.stop()
     clk = clocks.summary(t_host0, t_host1)
     ms_per_step = ms / args.steps
     tokens_per_step = n * len(layers)
-    value = world * tokens_per_step * args.steps / (ms / 1e3)
+    value = job_tokens_per_s(world, tokens_per_step, args.steps, ms)
 
     # ---- per-kernel timing (events recorded around each kernel, graph-replayed) ----
     n_lin = len(layers)
@@ -425,34 +463,41 @@ def ours(args):
     reps = max(3, min(50, args.steps // 20))
     g2.replay()
     torch.cuda.synchronize()
-    t_shr, t_gemm = [], []
+    t_shr = [[] for _ in range(n_lin)]
+    t_gemm = [[] for _ in range(n_lin)]
     for _ in range(reps):
         g2.replay()
         torch.cuda.synchronize()
-        for trio in evs:
-            t_shr.append(trio[0].elapsed_time(trio[1]))
-            t_gemm.append(trio[1].elapsed_time(trio[2]))
-    gemm_ms = statistics.mean(t_gemm)
-    shrink_ms = statistics.mean(t_shr)
+        for i, trio in enumerate(evs):
+            t_shr[i].append(trio[0].elapsed_time(trio[1]))
+            t_gemm[i].append(trio[1].elapsed_time(trio[2]))
+    gemm_ms_i = [statistics.mean(v) for v in t_gemm]
+    shrink_ms = statistics.mean(statistics.mean(v) for v in t_shr)
+    gemm_ms = statistics.mean(gemm_ms_i)
 
-    alg = algorithmic(None, idx.numpy(), desc)
+    idx_np = idx.numpy()
+    algs = [algorithmic_case(idx_np, c.h_in, c.h_out, c.adapters.r_max) for c in cases]
+    # per-linear roofline time: the slower of bytes at HBM bandwidth and FLOPs at tensor peak
+    step_roof_ms = sum(max(a_["linear_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                           a_["linear_flops"] / (peaks["bf16_tflops"] * 1e12)) for a_ in algs) * 1e3
+    alg = {"D": algs[0]["D"], "n_L": algs[0]["n_L"]}
     if args.workload == "prefill":
-        achieved = alg["gemm_flops"] / (gemm_ms / 1e3) / 1e12
+        achieved = sum(a_["gemm_flops"] for a_ in algs) / (sum(gemm_ms_i) / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": read_profile_traffic(f"gemm_prefill_{args.workload}"),
                 "kernel": "gemm_prefill_kernel", "kernel_ms": gemm_ms,
-                "algorithmic_flops_per_launch": alg["gemm_flops"], "peak_source": peaks["source"] + " burst",
+                "algorithmic_flops_per_launch": sum(a_["gemm_flops"] for a_ in algs) / n_lin,
+                "peak_source": peaks["source"] + " burst",
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
-        step_roof_ms = n_lin * alg["linear_flops"] / (peak * 1e12) * 1e3
     else:
-        achieved = alg["gemm_bytes"] / (gemm_ms / 1e3) / 1e9
+        achieved = sum(a_["gemm_bytes"] for a_ in algs) / (sum(gemm_ms_i) / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": read_profile_traffic(f"gemm_decode_{args.workload}"),
                 "kernel": "gemm_decode_kernel", "kernel_ms": gemm_ms,
-                "algorithmic_bytes_per_launch": alg["gemm_bytes"], "peak_source": peaks["source"] + " copy"}
-        step_roof_ms = n_lin * alg["linear_bytes"] / (peak * 1e9) * 1e3
+                "algorithmic_bytes_per_launch": sum(a_["gemm_bytes"] for a_ in algs) / n_lin,
+                "peak_source": peaks["source"] + " copy"}
     roof["shrink_ms"] = shrink_ms
     roof["step_roofline_ms"] = step_roof_ms
     roof["step_frac"] = step_roof_ms / ms_per_step
@@ -486,12 +531,9 @@ def ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * tokens_per_step * e2e_steps / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        e2e = {"value": job_tokens_per_s(world, tokens_per_step, e2e_steps, ems), "unit": UNIT,
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems / e2e_steps,
                "mode": "C-ABI calls captured in a CUDA graph; pinned host inputs copied in and outputs copied out "
                        "every step"}

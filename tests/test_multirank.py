@@ -1,0 +1,54 @@
+"""The replicas-only multi-GPU path of bench.py, run as two gloo ranks on the CPU.
+
+Each rank times its own batches; the job's throughput is the tokens of all ranks over the
+slowest rank's time, and every rank draws different batches (weak scaling)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, ms_of_rank, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(ms_of_rank[rank], dist)
+        idx, _, _ = bench.workload_cases("decode", rank, 1, 64, layer_range=range(0))
+        dist.barrier()
+        q.put((rank, ms, idx.tolist()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_max_and_distinct_batches():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    ms_of_rank = [3.0, 5.0]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, ms_of_rank, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=240) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    out.sort()
+    assert [o[1] for o in out] == [5.0, 5.0]  # every rank sees the slowest rank's time
+    assert out[0][2] != out[1][2]  # replicas draw different batches
+    assert bench.job_tokens_per_s(world, 64 * 32, 100, 5.0) == pytest.approx(2 * 64 * 32 * 100 / 5e-3)
+
+
+def test_single_process_helpers():
+    assert bench.max_over_ranks(7.5) == 7.5
+    assert bench.rank_seed_offset(0) == 0 and bench.rank_seed_offset(1) != 0
