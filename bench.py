@@ -385,7 +385,8 @@ def ours(args):
     idx_dev = idx.to(dev)
     pool0 = layers[0]["pool"]
     seg_ws = pool0.segment_workspace(n, dev)
-    lin_ws = pool0.linear_workspace(n, dev)
+    # one workspace serves every linear of the step (sequential on one stream): size it for the largest
+    lin_ws = ags._device_bytes(max(ags.lora_linear_workspace_bytes(L["pool"].handle, n) for L in layers), dev)
     torch.cuda.synchronize()
 
     launches_before = ags.lora_kernel_launch_count()
