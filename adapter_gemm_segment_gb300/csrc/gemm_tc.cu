@@ -43,7 +43,8 @@ constexpr int kThreads = 192;
 constexpr int kPrefillBN = 256;
 constexpr int kDecodeMaxN = 256;
 constexpr int kSmemBudget = 200 * 1024;
-constexpr int kLsmMaxTokens = 32;  // decode CTAs precompute the LoRA term when they own <= this many tokens
+constexpr int kLsmMaxTokens = 32;
+constexpr int kYChunk = 32;  // tokens per TMA store of the decode output  // decode CTAs precompute the LoRA term when they own <= this many tokens
 
 struct DecodeArgs {
     PoolView pool;
@@ -435,7 +436,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int g_begin = use_lsm ? a.dpre : 0;  // with L_sm the pre-staged group is already applied
         if (a.fuse && D > g_begin) {
             T* Blate = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128) +
-                       (size_t)per * BM;  // after the y tile
+                       (size_t)2 * kYChunk * BM;  // after the two y buffers
             const size_t late_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(Blate) - smem);
             const int dlate = max(1, static_cast<int>(late_bytes / ((size_t)BM * R * sizeof(T))));
             for (int g0 = g_begin; g0 < D;) {
@@ -478,53 +479,59 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         bool recv = true;
         if (push && cnt > 0 && a.splits > 1) recv = __all_sync(0xffffffffu, mbar_wait(rbar, 0, flags));
-        // the owned [cnt tokens][128 features] tile of y is assembled in shared memory (after the
-        // receive buffer) and written with one TMA store; rows/columns outside y are clipped
+        // y is assembled in shared memory 32 tokens at a time (two buffers of [32][128], after
+        // the receive buffer) and written with TMA stores; rows/columns outside y are clipped
         T* Ysm = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128);
-        if (recv) {
-            for (int q0 = 0; q0 < cnt; q0 += 8) {  // 8 tokens per batch, every load in flight first
-                float v[8];
+        for (int c0 = 0; c0 < cnt; c0 += kYChunk) {
+            T* Yb = Ysm + (size_t)((c0 / kYChunk) & 1) * kYChunk * BM;
+            named_bar_sync(1, 128);  // this buffer's previous TMA store has finished reading it
+            if (recv) {
+                for (int q0 = c0; q0 < min(cnt, c0 + kYChunk); q0 += 8) {  // 8 tokens, all loads first
+                    float v[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int q = min(q0 + u, cnt - 1);
-                    v[u] = own[q * BM + row];
-                    if (use_lsm) v[u] += L_sm[q * BM + row];
-                }
-                if (push) {
+                    for (int u = 0; u < 8; ++u) {
+                        const int q = min(q0 + u, cnt - 1);
+                        v[u] = own[q * BM + row];
+                        if (use_lsm) v[u] += L_sm[q * BM + row];
+                    }
+                    if (push) {
 #pragma unroll
-                    for (int c = 0; c < 7; ++c) {
-                        if (c < a.splits - 1) {
+                        for (int c = 0; c < 7; ++c) {
+                            if (c < a.splits - 1) {
+                                float r8[8];
+#pragma unroll
+                                for (int u = 0; u < 8; ++u)
+                                    r8[u] = Rcv[((size_t)c * per + min(q0 + u, cnt - 1)) * BM + row];
+#pragma unroll
+                                for (int u = 0; u < 8; ++u) v[u] += r8[u];
+                            }
+                        }
+                    } else {
+                        for (int c = 0; c < a.splits; ++c) {
+                            if (c == rank) continue;
                             float r8[8];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) r8[u] = Rcv[((size_t)c * per + min(q0 + u, cnt - 1)) * BM + row];
+                            for (int u = 0; u < 8; ++u)
+                                r8[u] = ld_dsmem_f32(mapa_shared(smem_u32(own + min(q0 + u, cnt - 1) * BM + row),
+                                                                 static_cast<uint32_t>(c)));
 #pragma unroll
                             for (int u = 0; u < 8; ++u) v[u] += r8[u];
                         }
                     }
-                } else {
-                    for (int c = 0; c < a.splits; ++c) {
-                        if (c == rank) continue;
-                        float r8[8];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            r8[u] = ld_dsmem_f32(mapa_shared(smem_u32(own + min(q0 + u, cnt - 1) * BM + row),
-                                                             static_cast<uint32_t>(c)));
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) v[u] += r8[u];
-                    }
+                    for (int u = 0; u < 8; ++u)
+                        if (q0 + u < cnt) Yb[(q0 + u - c0) * BM + row] = from_f32<T>(v[u]);
                 }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (q0 + u < cnt) Ysm[(q0 + u) * BM + row] = from_f32<T>(v[u]);
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (et == 0 && recv) {
+                tma_store_2d(&tmY, Yb, m_tile * BM, t0 + c0);
+                bulk_commit_group();
+                bulk_wait_group_read1();  // the other buffer is free again
+            }
         }
-        named_bar_sync(1, 128);
-        if (et == 0 && recv && cnt > 0) {
-            tma_store_2d(&tmY, Ysm, m_tile * BM, t0);
-            bulk_commit_group();
-            bulk_wait_group_read0();
-        }
+        if (et == 0) bulk_wait_group_read0();
     }
     tc_fence_before();
     cluster_sync();  // no CTA leaves while its parked rows may still be copied or read
@@ -775,7 +782,7 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     const size_t limit = 225 * 1024;
     // stage area after the main loop: P [n_pad][128] + receive buffer [splits-1][per][128]
     // (exchange by bulk copies) + one late B tile
-    const size_t ytile = (size_t)per * BM * 2 + 128;
+    const size_t ytile = (size_t)2 * kYChunk * BM * 2 + 128;
     const size_t park_push = (size_t)p.n_pad * BM * 4 + (size_t)(p.splits - 1) * per * BM * 4 + ytile + slot_b;
     const size_t park_pull = (size_t)p.n_pad * BM * 4 + ytile + slot_b;
     p.push = 1;
@@ -807,7 +814,7 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
 int tc_supported(const PoolView& pv, int n) {
     if (pv.dtype != LORA_F16 && pv.dtype != LORA_BF16) return 0;
     if (pv.h_in % 8 || pv.h_out % 8 || pv.R % 8) return 0;
-    if (n > 0 && n <= tc::kDecodeMaxN && tc::plan_decode(pv, n, (pv.h_in + 1023) / 1024).smem > (size_t)(227 * 1024))
+    if (n > 0 && n <= tc::kDecodeMaxN && tc::plan_decode(pv, n, shrink_parts(pv, n, false)).smem > (size_t)(227 * 1024))
         return 0;
     return 1;
 }
@@ -827,7 +834,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         rc = make_map(&mX, x, bf16, pv.h_in, n, p.n_pad);
         if (rc) return rc;
         const int per = (p.n_pad + p.splits - 1) / p.splits;
-        rc = make_map_plain(&mY, y, bf16, pv.h_out, n, BM, per);
+        rc = make_map_plain(&mY, y, bf16, pv.h_out, n, BM, kYChunk);
         if (rc) return rc;
         DecodeArgs a;
         a.pool = pv;

@@ -7,6 +7,8 @@
 // kernel (fused) or as a residual added by a second kernel (separate).  The shrink writes
 // s[t, j] = (alpha_s / r_s) * sum_k x[t,k] A_s[j,k] in float32 for every token t with a slot,
 // in original token order; both expands read it.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -70,9 +72,10 @@ shrink_warp_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* _
     }
 }
 
-// ---- shrink for small batches: one CTA per (token, 8 adapter rows, 1024 features) -------------
-// 128 threads each own 8 consecutive input features, so a CTA reads 2 KB of x and 16 KB of A
-// with all nine 16-byte loads of a thread in flight; the K-parts are summed by the consumers.
+// ---- shrink for small batches: one CTA per (token, 8 adapter rows, K-part) -------------------
+// 128 threads each own 8 consecutive input features of every 1024-feature sweep, so a sweep
+// reads 2 KB of x and 16 KB of A with all nine 16-byte loads of a thread in flight; the K-parts
+// (shrink_parts) are summed by the consumers.
 // The whole grid is resident at once for decode batches, so tokens are taken in their original
 // order (one dependent load less than walking the sorted order).
 constexpr int kShrKChunk = 1024;
@@ -87,21 +90,26 @@ shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* 
     pdl_trigger();
     const int t = blockIdx.x, g = blockIdx.y, ks = blockIdx.z;
     const int h = pool.h_in, R = pool.R;
-    const int k = ks * kShrKChunk + threadIdx.x * 8;
+    // this CTA's K range: part ks of gridDim.z, in sweeps of 1024 features (128 threads x 8)
+    const int sweeps = ((h + kShrKChunk - 1) / kShrKChunk + gridDim.z - 1) / gridDim.z;
+    const int k_beg = ks * sweeps * kShrKChunk;
+    const int k_end = min(h, k_beg + sweeps * kShrKChunk);
+    const int k0 = k_beg + threadIdx.x * 8;
     // independent loads first: status, slot, x; then the slot's A rows
     const int status = __ldcg(seg.status);
     const int s = __ldcg(seg.idx + t);
     uint4 xv = make_uint4(0, 0, 0, 0);
-    if (k < h) xv = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * h + k));
+    if (k0 < k_end) xv = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * h + k0));
     if (s < 0 || status != LORA_OK) return;
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.f;
-    if (k < h) {
-        const T* Ar = static_cast<const T*>(pool.A) + ((size_t)s * R + (size_t)g * 8) * h + k;
+    const T* Ab = static_cast<const T*>(pool.A) + ((size_t)s * R + (size_t)g * 8) * h;
+    for (int k = k0; k < k_end; k += kShrKChunk) {
+        if (k != k0) xv = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * h + k));
         uint4 av[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) av[r] = __ldg(reinterpret_cast<const uint4*>(Ar + (size_t)r * h));
+        for (int r = 0; r < 8; ++r) av[r] = __ldg(reinterpret_cast<const uint4*>(Ab + (size_t)r * h + k));
         float xf[8];
         unpack8<T>(xv, xf);
 #pragma unroll
@@ -345,10 +353,14 @@ gemm_simt_kernel(PoolView pool, SegView seg, const T* __restrict__ W, const T* _
 
 // ---- host launchers ----------------------------------------------------------------------------
 
+// K-parts of the small-batch shrink: enough CTAs to keep the loads in flight (~256 CTAs per
+// group of 8 adapter rows), at most 4 parts so that the consumers stage little.
 int shrink_parts(const PoolView& pv, int n, bool tiled) {
-    if (pv.dtype != LORA_F32 && !tiled) return (pv.h_in + kShrKChunk - 1) / kShrKChunk;
-    (void)n;
-    return 1;
+    if (pv.dtype == LORA_F32 || tiled) return 1;
+    int p = (pv.h_in + kShrKChunk - 1) / kShrKChunk;
+    p = std::min(p, 4);
+    p = std::min(p, std::max(1, 256 / std::max(n, 1)));
+    return p;
 }
 
 template <typename T>
