@@ -177,7 +177,8 @@ __device__ __forceinline__ void lora_batch8(const T* __restrict__ Bg, const floa
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ CUtensorMap tmY, const DecodeArgs a) {
+                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmYtail,
+                   const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
@@ -232,6 +233,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmY);
+        prefetch_tmap(&tmYtail);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, a.tmem_cols);
@@ -482,11 +484,14 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // y is assembled in shared memory 32 tokens at a time (two buffers of [32][128], after
         // the receive buffer) and written with TMA stores; rows/columns outside y are clipped
         T* Ysm = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128);
-        for (int c0 = 0; c0 < cnt; c0 += kYChunk) {
-            T* Yb = Ysm + (size_t)((c0 / kYChunk) & 1) * kYChunk * BM;
+        // store boxes never cross into the next CTA's tokens: ychunk = min(32, per) rows, and the
+        // last (per % ychunk)-row piece of a share goes through the tail map
+        const int ychunk = min(kYChunk, per);
+        for (int c0 = 0; c0 < cnt; c0 += ychunk) {
+            T* Yb = Ysm + (size_t)((c0 / ychunk) & 1) * kYChunk * BM;
             named_bar_sync(1, 128);  // this buffer's previous TMA store has finished reading it
             if (recv) {
-                for (int q0 = c0; q0 < min(cnt, c0 + kYChunk); q0 += 8) {  // 8 tokens, all loads first
+                for (int q0 = c0; q0 < min(cnt, c0 + ychunk); q0 += 8) {  // 8 tokens, all loads first
                     float v[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
@@ -520,13 +525,13 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     }
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
-                        if (q0 + u < cnt) Yb[(q0 + u - c0) * BM + row] = from_f32<T>(v[u]);
+                        if (q0 + u < min(cnt, c0 + ychunk)) Yb[(q0 + u - c0) * BM + row] = from_f32<T>(v[u]);
                 }
                 fence_proxy_async_smem();
             }
             named_bar_sync(1, 128);
             if (et == 0 && recv) {
-                tma_store_2d(&tmY, Yb, m_tile * BM, t0 + c0);
+                tma_store_2d(c0 + ychunk <= per ? &tmY : &tmYtail, Yb, m_tile * BM, t0 + c0);
                 bulk_commit_group();
                 bulk_wait_group_read1();  // the other buffer is free again
             }
@@ -834,7 +839,12 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         rc = make_map(&mX, x, bf16, pv.h_in, n, p.n_pad);
         if (rc) return rc;
         const int per = (p.n_pad + p.splits - 1) / p.splits;
-        rc = make_map_plain(&mY, y, bf16, pv.h_out, n, BM, kYChunk);
+        const int ychunk = std::min(kYChunk, per);
+        const int ytail = per % ychunk;
+        CUtensorMap mYt;
+        rc = make_map_plain(&mY, y, bf16, pv.h_out, n, BM, ychunk);
+        if (rc) return rc;
+        rc = make_map_plain(&mYt, y, bf16, pv.h_out, n, BM, ytail ? ytail : ychunk);
         if (rc) return rc;
         DecodeArgs a;
         a.pool = pv;
@@ -861,7 +871,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
                                                227 * 1024));
             attr_set = true;
         }
-        void* args[] = {(void*)&mW, (void*)&mX, (void*)&mY, (void*)&a};
+        void* args[] = {(void*)&mW, (void*)&mX, (void*)&mY, (void*)&mYt, (void*)&a};
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(p.m_tiles, p.splits);
