@@ -52,6 +52,7 @@ struct DecodeArgs {
     const float* s_in;
     void* y;
     int n, n_pad, kb_total, splits, kb_per_split, stages, tmem_cols, fuse, bf16;
+    int nacc;     // independent TMEM accumulators the K-blocks rotate over (summed in the epilogue)
     int s_parts;  // K-parts of the shrink output to sum
     int dpre;     // distinct slots whose B rows are staged during the main loop
     int push;     // exchange partials by bulk copies (1) or remote loads (0)
@@ -276,6 +277,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
     } else if (warp == 1) {
         if (lane == 0) {
+            // With only n_pad tokens on N an MMA is short, and a chain of MMAs into one
+            // accumulator waits on each other; K-blocks therefore rotate over nacc accumulators.
             const uint32_t idesc = idesc_f16(BM, a.n_pad, a.bf16 != 0);
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % stages;
@@ -286,10 +289,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 tc_fence_after();
                 const uint32_t wa = smem_u32(smem + s * stage_bytes);
                 const uint32_t xa = wa + w_bytes;
+                const uint32_t acc = tmem + static_cast<uint32_t>((i % a.nacc) * a.n_pad);
 #pragma unroll
                 for (int k = 0; k < BK / UMMA_K; ++k)
-                    umma_f16(tmem, sdesc_sw128(wa + k * UMMA_K * 2), sdesc_sw128(xa + k * UMMA_K * 2), idesc,
-                             (i > 0 || k > 0) ? 1u : 0u);
+                    umma_f16(acc, sdesc_sw128(wa + k * UMMA_K * 2), sdesc_sw128(xa + k * UMMA_K * 2), idesc,
+                             (i >= a.nacc || k > 0) ? 1u : 0u);
                 umma_commit(&empty[s]);
             }
             umma_commit(tmem_full);  // also on abort: fires once the issued MMAs have finished
@@ -401,13 +405,21 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         named_bar_sync(1, 128);
         if (flags[1]) {
             const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const int used = min(a.nacc, nkb);  // accumulators that received K-blocks
             for (int c0 = 0; c0 < a.n_pad && c0 < n; c0 += 16) {
-                uint32_t r[16];
-                __syncwarp();
-                tmem_ld16(taddr + c0, r);
-                tmem_ld_wait();
+                float v[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) P[(c0 + c) * BM + row] = __uint_as_float(r[c]);
+                for (int c = 0; c < 16; ++c) v[c] = 0.f;
+                for (int j = 0; j < used; ++j) {
+                    uint32_t r[16];
+                    __syncwarp();
+                    tmem_ld16(taddr + static_cast<uint32_t>(j * a.n_pad) + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
+                }
+#pragma unroll
+                for (int c = 0; c < 16; ++c) P[(c0 + c) * BM + row] = v[c];
             }
             fence_proxy_async_smem();  // the parked rows are read by bulk copies
         }
@@ -758,7 +770,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 // ============================================================================================
 
 struct DecodePlan {
-    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre, push, s_parts;
+    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre, push, s_parts, nacc;
     size_t smem;
 };
 
@@ -807,8 +819,10 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
         }
     }
     if (!p.stages) p.stages = 8;  // does not fit: tc_supported rejects the shape
+    // up to 4 accumulators of n_pad columns within half of the 512 TMEM columns
+    p.nacc = std::max(1, std::min(4, 256 / p.n_pad));
     int cols = 32;
-    while (cols < p.n_pad) cols <<= 1;
+    while (cols < p.n_pad * p.nacc) cols <<= 1;
     p.tmem_cols = cols;
     p.smem = (size_t)p.stages * stage_bytes + fixed + (size_t)p.dpre * slot_b + 1024;
     return p;
@@ -858,6 +872,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.kb_per_split = p.kb_per_split;
         a.stages = p.stages;
         a.tmem_cols = p.tmem_cols;
+        a.nacc = p.nacc;
         a.fuse = fuse ? 1 : 0;
         a.bf16 = bf16;
         a.s_parts = s_parts;
