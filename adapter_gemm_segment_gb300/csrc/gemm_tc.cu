@@ -44,7 +44,8 @@ constexpr int kPrefillBN = 256;
 constexpr int kDecodeMaxN = 256;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kLsmMaxTokens = 32;
-constexpr int kYChunk = 32;  // tokens per TMA store of the decode output  // decode CTAs precompute the LoRA term when they own <= this many tokens
+constexpr int kYChunk = 32;  // tokens per TMA store of the decode output
+constexpr int kDecIssuers = 5;  // producer lanes of the decode kernel (4 W quarters + x)  // decode CTAs precompute the LoRA term when they own <= this many tokens
 
 struct DecodeArgs {
     PoolView pool;
@@ -53,6 +54,7 @@ struct DecodeArgs {
     void* y;
     int n, n_pad, kb_total, splits, kb_per_split, stages, tmem_cols, fuse, bf16;
     int nacc;     // independent TMEM accumulators the K-blocks rotate over (summed in the epilogue)
+    int kc;       // 64-wide K chunks per pipeline stage (one TMA box per operand and stage)
     int s_parts;  // K-parts of the shrink output to sum
     int dpre;     // distinct slots whose B rows are staged during the main loop
     int push;     // exchange partials by bulk copies (1) or remote loads (0)
@@ -183,8 +185,9 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
-    const uint32_t w_bytes = BM * BK * 2;
-    const uint32_t x_bytes = static_cast<uint32_t>(a.n_pad) * BK * 2;
+    const int kc = a.kc;
+    const uint32_t w_bytes = BM * BK * 2 * kc;
+    const uint32_t x_bytes = static_cast<uint32_t>(a.n_pad) * BK * 2 * kc;
     const uint32_t stage_bytes = w_bytes + x_bytes;
     const int R = a.pool.R;
     const int per = (a.n_pad + a.splits - 1) / a.splits;  // tokens reduced by each CTA
@@ -207,8 +210,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, split = blockIdx.y;
+    // K range of this split in 64-wide blocks, walked in stages of kc blocks
     const int kb0 = split * a.kb_per_split;
-    const int nkb = min(a.kb_total, kb0 + a.kb_per_split) - kb0;
+    const int nkb = (min(a.kb_total, kb0 + a.kb_per_split) - kb0 + kc - 1) / kc;  // stages
+    // Every feature tile reads the same x slice; starting each tile's walk over its K range at a
+    // different stage keeps the concurrent reads of x spread over different lines.
+    const int kb_rot = nkb > 0 ? m_tile % nkb : 0;
     const int n = a.n, h_out = a.pool.h_out;
     const int rank = static_cast<int>(cluster_ctarank());
     const int t0 = rank * per;
@@ -253,17 +260,23 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const T* B = static_cast<const T*>(a.pool.B);
 
     if (warp == 0) {
+        // W and x are complete when this grid starts: the shrink kernel that precedes it in the
+        // stream releases its dependents only after its own grid-dependency wait.  Only the
+        // shrink output (read by the epilogue warps) needs this grid's wait.
         if (lane == 0) {
-            // W and x are complete when this grid starts: the shrink kernel that precedes it in
-            // the stream releases its dependents only after its own grid-dependency wait.  Only
-            // the shrink output (read by the epilogue warps) needs this grid's wait.
             int issued = 0;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % stages;
                 if (i >= stages && !mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
+                const int kb = kb0 + ((i + kb_rot) % nkb) * kc;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
-                tma_load_2d(smem + s * stage_bytes, &tmW, &full[s], (kb0 + i) * BK, m_tile * BM);
-                tma_load_2d(smem + s * stage_bytes + w_bytes, &tmX, &full[s], (kb0 + i) * BK, 0);
+                if (kc == 1) {
+                    tma_load_2d_cta(smem + s * stage_bytes, &tmW, &full[s], kb * BK, m_tile * BM);
+                    tma_load_2d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], kb * BK, 0);
+                } else {
+                    tma_load_3d_cta(smem + s * stage_bytes, &tmW, &full[s], 0, m_tile * BM, kb);
+                    tma_load_3d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], 0, 0, kb);
+                }
                 ++issued;
             }
             if (flags[0]) {  // aborted: let copies already in flight land before the CTA exits
@@ -290,10 +303,13 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 const uint32_t wa = smem_u32(smem + s * stage_bytes);
                 const uint32_t xa = wa + w_bytes;
                 const uint32_t acc = tmem + static_cast<uint32_t>((i % a.nacc) * a.n_pad);
+                for (int c = 0; c < kc; ++c) {
+                    const uint32_t wc = wa + c * BM * BK * 2, xc = xa + c * a.n_pad * BK * 2;
 #pragma unroll
-                for (int k = 0; k < BK / UMMA_K; ++k)
-                    umma_f16(acc, sdesc_sw128(wa + k * UMMA_K * 2), sdesc_sw128(xa + k * UMMA_K * 2), idesc,
-                             (i >= a.nacc || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        umma_f16(acc, sdesc_sw128(wc + k * UMMA_K * 2), sdesc_sw128(xc + k * UMMA_K * 2), idesc,
+                                 (i >= a.nacc || c > 0 || k > 0) ? 1u : 0u);
+                }
                 umma_commit(&empty[s]);
             }
             umma_commit(tmem_full);  // also on abort: fires once the issued MMAs have finished
@@ -770,7 +786,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 // ============================================================================================
 
 struct DecodePlan {
-    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre, push, s_parts, nacc;
+    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre, push, s_parts, nacc, kc;
     size_t smem;
 };
 
@@ -786,9 +802,13 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     splits = std::min(splits, 8);  // portable cluster size
     splits = std::min(splits, std::max(1, p.kb_total / 4));
     p.kb_per_split = (p.kb_total + splits - 1) / splits;
+    // two 64-wide K chunks per stage (one TMA box per operand) when the K split allows it
+    // (measured on GB300: no gain over one chunk per stage, so one chunk is used; the
+    // two-chunk path stays tested by setting kc = 2 here)
+    p.kc = 1;
     p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
     const int per = (p.n_pad + p.splits - 1) / p.splits;
-    const size_t stage_bytes = (size_t)BM * BK * 2 + (size_t)p.n_pad * BK * 2;
+    const size_t stage_bytes = ((size_t)BM * BK * 2 + (size_t)p.n_pad * BK * 2) * p.kc;
     const bool use_lsm = per <= kLsmMaxTokens;
     // dedicated region: 4 int arrays, s parts [s_parts][per][R], LoRA term [per][128] (small
     // shares), alignment, barriers
@@ -809,7 +829,7 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
         const size_t park = pass == 0 ? park_push : park_pull;
         int min_stages = 2;
         while ((size_t)min_stages * stage_bytes < park) ++min_stages;
-        for (int st = std::max(8, min_stages); st >= std::max(3, min_stages); --st) {
+        for (int st = std::max(8, min_stages); st >= std::max(p.kc == 2 ? 2 : 3, min_stages); --st) {
             if ((size_t)st * stage_bytes + fixed > limit) continue;
             const int dp = (int)std::min<size_t>((size_t)want, (limit - st * stage_bytes - fixed) / slot_b);
             p.stages = st;
@@ -819,8 +839,9 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
         }
     }
     if (!p.stages) p.stages = 8;  // does not fit: tc_supported rejects the shape
-    // up to 4 accumulators of n_pad columns within half of the 512 TMEM columns
-    p.nacc = std::max(1, std::min(4, 256 / p.n_pad));
+    // One accumulator: rotating K-blocks over several (to break the MMA dependency chain)
+    // was measured and gave no gain on GB300; the mechanism stays for shapes where it might.
+    p.nacc = 1;
     int cols = 32;
     while (cols < p.n_pad * p.nacc) cols <<= 1;
     p.tmem_cols = cols;
@@ -848,9 +869,16 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     if (n <= kDecodeMaxN) {
         const DecodePlan p = plan_decode(pv, n, s_parts);
         CUtensorMap mW, mX, mY;
-        int rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, BM);
-        if (rc) return rc;
-        rc = make_map(&mX, x, bf16, pv.h_in, n, p.n_pad);
+        int rc;
+        if (p.kc == 2) {
+            rc = make_map_chunked(&mW, W, bf16, pv.h_in, pv.h_out, BM, 2);
+            if (rc) return rc;
+            rc = make_map_chunked(&mX, x, bf16, pv.h_in, n, p.n_pad, 2);
+        } else {
+            rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, BM);
+            if (rc) return rc;
+            rc = make_map(&mX, x, bf16, pv.h_in, n, p.n_pad);
+        }
         if (rc) return rc;
         const int per = (p.n_pad + p.splits - 1) / p.splits;
         const int ychunk = std::min(kYChunk, per);
@@ -873,6 +901,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.stages = p.stages;
         a.tmem_cols = p.tmem_cols;
         a.nacc = p.nacc;
+        a.kc = p.kc;
         a.fuse = fuse ? 1 : 0;
         a.bf16 = bf16;
         a.s_parts = s_parts;

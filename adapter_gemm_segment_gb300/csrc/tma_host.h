@@ -39,6 +39,26 @@ inline int make_map(CUtensorMap* m, const void* base, int bf16, uint64_t cols, u
     return LORA_OK;
 }
 
+// Row-major [rows, cols] 16-bit matrix seen as [chunks][rows][64] (chunk = 64 columns, so the
+// chunk stride is 128 bytes): one box {64, box_rows, box_chunks} lands as box_chunks
+// consecutive [box_rows][64] tiles with 128-byte swizzle -- the layout of box_chunks
+// consecutive 2-D boxes, fetched by a single TMA instruction.  cols must be a multiple of 64.
+inline int make_map_chunked(CUtensorMap* m, const void* base, int bf16, uint64_t cols, uint64_t rows,
+                            uint32_t box_rows, uint32_t box_chunks) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[3] = {64, rows, cols / 64};
+    const cuuint64_t strides[2] = {cols * 2, 128};
+    const cuuint32_t box[3] = {64u, box_rows, box_chunks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled (chunked) failed (%d)", (int)r);
+    return LORA_OK;
+}
+
 // Row-major [rows, cols] 16-bit matrix, box {box_cols, box_rows}, no swizzle (for stores of
 // row-major shared-memory tiles).
 inline int make_map_plain(CUtensorMap* m, const void* base, int bf16, uint64_t cols, uint64_t rows, uint32_t box_cols,
