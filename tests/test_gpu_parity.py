@@ -202,6 +202,9 @@ SMALL = [
     (17, 300, 512, 256, [16, 3, 16], 16, torch.bfloat16),
     (18, 700, 136, 392, [8, 8], 8, torch.float16),
     (19, 129, 4104, 64, [8, 8], 8, torch.bfloat16),
+    # two K chunks per decode stage: whole stages, and a split whose last stage is half past h_in
+    (20, 64, 1024, 256, [8, 8], 8, torch.bfloat16),
+    (21, 40, 704, 136, [8, 16, 16], 16, torch.float16),
 ]
 
 
