@@ -45,6 +45,7 @@ constexpr int kDecodeMaxN = 256;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kLsmMaxTokens = 32;
 constexpr int kYChunk = 32;  // tokens per TMA store of the decode output
+constexpr int kYBatch = 16;  // tokens whose partials one epilogue thread loads before adding them
 
 struct DecodeArgs {
     PoolView pool;
@@ -411,7 +412,6 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (size_t off = beg; off < end; off += 65536)
                 prefetch_l2_bulk(a.prefetch + off, static_cast<uint32_t>(end - off < 65536 ? end - off : 65536));
         }
-        named_bar_sync(1, 128);
         if (et == 0) {
             flags[1] = (got && !flags[0] && flags[3] == LORA_OK) ? 1 : 0;
             // receive buffer: one bulk copy of this CTA's token rows from every other CTA
@@ -421,20 +421,30 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         if (flags[1]) {
             const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             const int used = min(a.nacc, nkb);  // accumulators that received K-blocks
-            for (int c0 = 0; c0 < a.n_pad && c0 < n; c0 += 16) {
-                float v[16];
+            const int cols = min(a.n_pad, (n + 15) & ~15);
+            // 64 columns per round: all TMEM loads of the round, one wait, then the stores
+            // (one warp per scheduler runs this, so serial load-wait-store rounds are slow)
+            for (int c0 = 0; c0 < cols; c0 += 64) {
+                float v[64];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) v[c] = 0.f;
+                for (int c = 0; c < 64; ++c) v[c] = 0.f;
                 for (int j = 0; j < used; ++j) {
-                    uint32_t r[16];
+                    uint32_t r[64];
                     __syncwarp();
-                    tmem_ld16(taddr + static_cast<uint32_t>(j * a.n_pad) + c0, r);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (c0 + 16 * q < cols)
+                            tmem_ld16(taddr + static_cast<uint32_t>(j * a.n_pad + c0 + 16 * q),
+                                      *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
+                    for (int c = 0; c < 64; ++c) v[c] += __uint_as_float(r[c]);
                 }
 #pragma unroll
-                for (int c = 0; c < 16; ++c) P[(c0 + c) * BM + row] = v[c];
+                for (int q = 0; q < 4; ++q)
+                    if (c0 + 16 * q < cols)
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) P[(c0 + 16 * q + c) * BM + row] = v[16 * q + c];
             }
             fence_proxy_async_smem();  // the parked rows are read by bulk copies
         }
@@ -518,10 +528,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             T* Yb = Ysm + (size_t)((c0 / ychunk) & 1) * kYChunk * BM;
             named_bar_sync(1, 128);  // this buffer's previous TMA store has finished reading it
             if (recv) {
-                for (int q0 = c0; q0 < min(cnt, c0 + ychunk); q0 += 8) {  // 8 tokens, all loads first
-                    float v[8];
+                for (int q0 = c0; q0 < min(cnt, c0 + ychunk); q0 += kYBatch) {  // kYBatch tokens, all loads first
+                    float v[kYBatch];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
+                    for (int u = 0; u < kYBatch; ++u) {
                         const int q = min(q0 + u, cnt - 1);
                         v[u] = own[q * BM + row];
                         if (use_lsm) v[u] += L_sm[q * BM + row];
@@ -530,28 +540,28 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 #pragma unroll
                         for (int c = 0; c < 7; ++c) {
                             if (c < a.splits - 1) {
-                                float r8[8];
+                                float r8[kYBatch];
 #pragma unroll
-                                for (int u = 0; u < 8; ++u)
+                                for (int u = 0; u < kYBatch; ++u)
                                     r8[u] = Rcv[((size_t)c * per + min(q0 + u, cnt - 1)) * BM + row];
 #pragma unroll
-                                for (int u = 0; u < 8; ++u) v[u] += r8[u];
+                                for (int u = 0; u < kYBatch; ++u) v[u] += r8[u];
                             }
                         }
                     } else {
                         for (int c = 0; c < a.splits; ++c) {
                             if (c == rank) continue;
-                            float r8[8];
+                            float r8[kYBatch];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
+                            for (int u = 0; u < kYBatch; ++u)
                                 r8[u] = ld_dsmem_f32(mapa_shared(smem_u32(own + min(q0 + u, cnt - 1) * BM + row),
                                                                  static_cast<uint32_t>(c)));
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) v[u] += r8[u];
+                            for (int u = 0; u < kYBatch; ++u) v[u] += r8[u];
                         }
                     }
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
+                    for (int u = 0; u < kYBatch; ++u)
                         if (q0 + u < min(cnt, c0 + ychunk)) Yb[(q0 + u - c0) * BM + row] = from_f32<T>(v[u]);
                 }
                 fence_proxy_async_smem();
