@@ -51,7 +51,7 @@ class lora_pool_desc(ctypes.Structure):
 class lora_segments(ctypes.Structure):
     _fields_ = [("perm_dev", ctypes.c_void_p), ("seg_start_dev", ctypes.c_void_p), ("seg_slot_dev", ctypes.c_void_p),
                 ("nseg_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p), ("idx_dev", ctypes.c_void_p),
-                ("n_tokens", ctypes.c_int32), ("n_slots", ctypes.c_int32)]
+                ("items_dev", ctypes.c_void_p), ("n_tokens", ctypes.c_int32), ("n_slots", ctypes.c_int32)]
 
 
 def _load() -> ctypes.CDLL:
@@ -239,8 +239,8 @@ def segment_arrays(seg: lora_segments) -> dict:
         return ws[off:off + 4 * count].view(torch.int32)
 
     return {"perm": view(seg.perm_dev, n), "seg_start": view(seg.seg_start_dev, S + 2),
-            "seg_slot": view(seg.seg_slot_dev, S + 1), "nseg": view(seg.nseg_dev, 1),
-            "status": view(seg.status_dev, 1), "idx": view(seg.idx_dev, n)}
+            "seg_slot": view(seg.seg_slot_dev, S + 1), "nseg": view(seg.nseg_dev, 2),
+            "status": view(seg.status_dev, 1), "idx": view(seg.idx_dev, n), "items": view(seg.items_dev, 8 * n)}
 
 
 # ---- convenience ----------------------------------------------------------------------------

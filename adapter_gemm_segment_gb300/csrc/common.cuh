@@ -54,6 +54,7 @@ struct SegView {
     const int32_t* nseg;
     int32_t* status;
     const int32_t* idx;
+    const int32_t* items;  // [n][8] {slot, count, token[4]}; nseg[1] = number of items
     int n;
 };
 
@@ -65,6 +66,7 @@ inline SegView seg_view(const lora_segments* s) {
     v.nseg = s->nseg_dev;
     v.status = s->status_dev;
     v.idx = s->idx_dev;
+    v.items = s->items_dev;
     v.n = s->n_tokens;
     return v;
 }

@@ -90,11 +90,13 @@ __global__ void pool_load_kernel(const T* __restrict__ A_src, const T* __restric
 // One CTA of 1024 threads.  Shared memory: cnt[K], off[K], wcnt[32][K] (uint16) with
 // K = S + 1 keys (key k+1 for slot k, key 0 for idx -1).
 constexpr int kSegThreads = 1024;
+constexpr int kItemTok = 4;  // sorted tokens per shrink work item
 
 __global__ void __launch_bounds__(kSegThreads, 1)
 segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restrict__ table, int S,
                int32_t* __restrict__ perm, int32_t* __restrict__ seg_start, int32_t* __restrict__ seg_slot,
-               int32_t* __restrict__ nseg_out, int32_t* __restrict__ status, int32_t* __restrict__ idx_copy) {
+               int32_t* __restrict__ nseg_out, int32_t* __restrict__ status, int32_t* __restrict__ idx_copy,
+               int32_t* __restrict__ items) {
     extern __shared__ __align__(16) int smem_i[];
     const int K = S + 1;
     int* cnt = smem_i;
@@ -121,7 +123,8 @@ segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restri
     if (bad) {
         if (tid == 0) {
             *status = LORA_EIDX;
-            *nseg_out = 0;
+            nseg_out[0] = 0;
+            nseg_out[1] = 0;
             seg_start[0] = 0;
         }
         pdl_trigger();
@@ -182,11 +185,46 @@ segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restri
         }
         __syncthreads();
     }
+
+    // 4. shrink work items: key k >= 1 (slot k-1) gives ceil(cnt[k] / 4) runs of up to 4
+    //    consecutive sorted tokens; off[k] is now the end of key k's range
+    int* ibase = reinterpret_cast<int*>(wcnt);  // [K], free again
+    if (warp == 0) {
+        int run = 0;
+        for (int base = 0; base < K; base += 32) {
+            const int i = base + lane;
+            const int c = (i < K && i > 0) ? (cnt[i] + kItemTok - 1) / kItemTok : 0;
+            int v = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, d);
+                if (lane >= d) v += u;
+            }
+            if (i < K) ibase[i] = run + v - c;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) nseg_out[1] = run;
+    }
+    __syncthreads();
+    for (int j = tid; j < n; j += kSegThreads) {
+        const int t = perm[j];
+        const int key = idx[t] + 1;
+        if (key == 0) continue;
+        const int rel = j - (off[key] - cnt[key]);
+        int32_t* it = items + (size_t)(ibase[key] + rel / kItemTok) * 8;
+        it[2 + rel % kItemTok] = t;
+        if (rel % kItemTok == 0) {
+            const int nt = min(kItemTok, cnt[key] - rel);
+            it[0] = key - 1;
+            it[1] = nt;
+            for (int u = nt; u < kItemTok; ++u) it[2 + u] = t;  // padding: a valid token
+        }
+    }
     pdl_trigger();
 }
 
 struct SegLayout {
-    size_t perm, seg_start, seg_slot, nseg, status, idx, total;
+    size_t perm, seg_start, seg_slot, nseg, status, idx, items, total;
 };
 
 static SegLayout seg_layout(int n, int S) {
@@ -204,6 +242,8 @@ static SegLayout seg_layout(int n, int S) {
     o += 256;
     L.idx = o;
     o += align256(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    L.items = o;
+    o += align256(sizeof(int32_t) * 8 * (size_t)(n > 0 ? n : 1));
     L.total = o;
     return L;
 }
@@ -321,6 +361,7 @@ int lora_segment(const int32_t* idx_dev, int n_tokens, lora_pool_t pool, void* w
     out->nseg_dev = reinterpret_cast<int32_t*>(w + L.nseg);
     out->status_dev = reinterpret_cast<int32_t*>(w + L.status);
     out->idx_dev = reinterpret_cast<int32_t*>(w + L.idx);
+    out->items_dev = reinterpret_cast<int32_t*>(w + L.items);
     out->n_tokens = n_tokens;
     out->n_slots = S;
 
@@ -339,7 +380,7 @@ int lora_segment(const int32_t* idx_dev, int n_tokens, lora_pool_t pool, void* w
     int S_arg = S;
     void* args[] = {(void*)&idx_arg, (void*)&n_arg, (void*)&table_arg, (void*)&S_arg, (void*)&out->perm_dev,
                     (void*)&out->seg_start_dev, (void*)&out->seg_slot_dev, (void*)&out->nseg_dev,
-                    (void*)&out->status_dev, (void*)&out->idx_dev};
+                    (void*)&out->status_dev, (void*)&out->idx_dev, (void*)&out->items_dev};
     LORA_CUDA_TRY(launch_pdl((const void*)segment_kernel, dim3(1), dim3(kSegThreads), smem, (cudaStream_t)stream, args));
     return LORA_OK;
 }

@@ -94,9 +94,11 @@ typedef struct lora_pool* lora_pool_t;
  *   perm_dev[j]       original position of the j-th token in sorted order     [n]
  *   seg_start_dev[i]  first sorted position of segment i; seg_start[nseg] = n  [n_slots+2]
  *   seg_slot_dev[i]   slot of segment i (-1 for the base-only run)            [n_slots+1]
- *   nseg_dev          number of segments                                      [1]
+ *   nseg_dev          number of segments, then the number of shrink items    [2]
  *   status_dev        LORA_OK or LORA_EIDX                                    [1]
  *   idx_dev           copy of the batch's idx (original order)               [n]
+ *   items_dev         shrink work items: every adapter segment cut into runs of up to 4
+ *                     sorted tokens, {slot, count, token[4], 0, 0} each   [n][8]
  * Segments are rebuilt once per batch and reused by every linear layer that runs
  * over that batch, as long as the workspace stays alive and unmodified. */
 typedef struct {
@@ -106,6 +108,7 @@ typedef struct {
     int32_t* nseg_dev;
     int32_t* status_dev;
     int32_t* idx_dev;
+    int32_t* items_dev;
     int32_t n_tokens;
     int32_t n_slots;
 } lora_segments;

@@ -71,6 +71,18 @@ def check_segments(ags, seg, idx, S):
     assert np.array_equal(got["seg_start"][:nseg + 1], ss)
     assert np.array_equal(got["seg_slot"][:nseg], sl)
     assert np.array_equal(got["idx"], np.asarray(idx))
+    # shrink work items: every adapter segment cut into runs of up to 4 sorted tokens,
+    # {slot, count, tokens, padded with the run's first token}; derived from the segments
+    want = []
+    for i in range(nseg):
+        if sl[i] < 0:
+            continue
+        for j0 in range(ss[i], ss[i + 1], 4):
+            toks = [int(t) for t in perm[j0:min(j0 + 4, ss[i + 1])]]
+            want.append([int(sl[i]), len(toks)] + toks + [toks[0]] * (4 - len(toks)))
+    assert int(got["nseg"][1]) == len(want)
+    items = got["items"].reshape(-1, 8)[:len(want), :6]
+    assert np.array_equal(items, np.array(want, dtype=np.int32).reshape(-1, 6))
 
 
 # ------------------------------------------------------------------------------------------
@@ -205,6 +217,8 @@ SMALL = [
     # two K chunks per decode stage: whole stages, and a split whose last stage is half past h_in
     (20, 64, 1024, 256, [8, 8], 8, torch.bfloat16),
     (21, 40, 704, 136, [8, 16, 16], 16, torch.float16),
+    # r_max 64 at 100 tokens: the segmented shrink (4-token items), ragged K (4104 features)
+    (22, 100, 4104, 64, [64, 8, 16, 64, 1], 64, torch.bfloat16),
 ]
 
 
