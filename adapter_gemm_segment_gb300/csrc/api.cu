@@ -114,7 +114,15 @@ int lora_linear_workspace_bytes(lora_pool_t pool, int n_tokens, size_t* bytes) {
 
 int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant) {
     if (!pool || !variant) return set_error(LORA_EINVAL, "pool/variant is NULL");
-    *variant = n_tokens >= kFusedMinTokens ? LORA_VARIANT_FUSED : LORA_VARIANT_SEPARATE;
+    // Measured on GB300 (32 chained linears per step): fused wins from one token up as long
+    // as the decode GEMM stages every adapter its CTAs meet; past that the separate variant
+    // (base GEMM + segmented expand) is faster.  Prefill batches (> 256 tokens) are fused.
+    const PoolView pv = pool_view(pool);
+    if (n_tokens < kFusedMinTokens) *variant = LORA_VARIANT_SEPARATE;
+    else if (n_tokens <= 256 && tc_supported(pv, n_tokens) && !decode_fused_fits(pv, n_tokens))
+        *variant = LORA_VARIANT_SEPARATE;
+    else
+        *variant = LORA_VARIANT_FUSED;
     return LORA_OK;
 }
 

@@ -870,6 +870,18 @@ int tc_supported(const PoolView& pv, int n) {
     return 1;
 }
 
+// Whether the fused decode GEMM stages, during its main loop, the B rows of every adapter a
+// CTA's tokens can use (at most 32 owned tokens and pre-staged slots >= min(owned tokens,
+// n_slots)).  Otherwise its epilogue would load the rest in late SIMT groups, which measured
+// 1.1-2.3x slower than the separate variant (GB300: 7B layer at 256 tokens, r_max 64 at 128
+// and 256 tokens).
+int decode_fused_fits(const PoolView& pv, int n) {
+    if (n <= 0 || n > tc::kDecodeMaxN || !tc_supported(pv, n)) return 0;
+    const tc::DecodePlan p = tc::plan_decode(pv, n, shrink_parts(pv, n, false));
+    const int per = (p.n_pad + p.splits - 1) / p.splits;
+    return per <= tc::kLsmMaxTokens && p.dpre >= std::min(per, pv.S) ? 1 : 0;
+}
+
 template <typename T>
 static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
                        int s_parts, void* y, bool fuse, const void* prefetch, size_t prefetch_bytes, cudaStream_t st) {

@@ -15,6 +15,10 @@ int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s
                   int* s_parts);
 int shrink_parts(const PoolView& pv, int n, bool tiled);
 
+// Whether the fused tensor-core decode GEMM (n <= 256) holds every adapter's B rows a CTA can
+// need in shared memory during its main loop (the variant policy keys on this).
+int decode_fused_fits(const PoolView& pv, int n);
+
 // y[t, :] += s[t, :] B_s^T (separate variant's residual kernel).
 int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, int s_parts, void* y, cudaStream_t st);
 

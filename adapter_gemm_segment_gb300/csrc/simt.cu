@@ -369,6 +369,55 @@ expand_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, int s_
     }
 }
 
+// Segmented expand (separate variant, 16-bit): one CTA per (work item = up to 4 sorted tokens
+// of one adapter segment, 256 output features).  A thread loads its feature's B row of the
+// item's adapter once (r_max / 8 16-byte loads) and the item's y values, all before use, and
+// adds the LoRA term of every token of the item.
+template <typename T>
+__global__ void __launch_bounds__(256)
+expand_seg_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, int s_parts, T* __restrict__ y) {
+    extern __shared__ float ss[];  // [4][R]: the item's shrink rows (K parts summed)
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x;
+    const int status = __ldcg(seg.status);
+    const int n_items = __ldcg(seg.nseg + 1);
+    const int4 head = __ldcg(reinterpret_cast<const int4*>(seg.items + (size_t)b * 8));      // slot, count, tok0, tok1
+    const int2 tail = __ldcg(reinterpret_cast<const int2*>(seg.items + (size_t)b * 8 + 4));  // tok2, tok3
+    if (status != LORA_OK || b >= n_items) return;
+    const int R = pool.R, h_out = pool.h_out, slot = head.x, nt = head.y;
+    const int tok[kItemTok] = {head.z, head.w, tail.x, tail.y};
+    for (int e = threadIdx.x; e < kItemTok * R; e += blockDim.x) {
+        const int u = e / R, j = e - u * R;
+        float v = 0.f;
+        if (u < nt)
+            for (int k = 0; k < s_parts; ++k) v += __ldcg(s_in + ((size_t)k * seg.n + tok[u]) * R + j);
+        ss[e] = v;
+    }
+    const int o = blockIdx.y * 256 + threadIdx.x;
+    const bool live = o < h_out;
+    float yv[kItemTok];
+#pragma unroll
+    for (int u = 0; u < kItemTok; ++u) yv[u] = live && u < nt ? to_f32(y[(size_t)tok[u] * h_out + o]) : 0.f;
+    __syncthreads();
+    if (!live) return;
+    const T* Br = static_cast<const T*>(pool.B) + ((size_t)slot * h_out + o) * R;
+    float acc[kItemTok];
+#pragma unroll
+    for (int u = 0; u < kItemTok; ++u) acc[u] = 0.f;
+    for (int j = 0; j < R; j += 8) {
+        float bf[8];
+        unpack8<T>(__ldg(reinterpret_cast<const uint4*>(Br + j)), bf);
+#pragma unroll
+        for (int u = 0; u < kItemTok; ++u)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[u] = fmaf(bf[e], ss[u * R + j + e], acc[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kItemTok; ++u)
+        if (u < nt) y[(size_t)tok[u] * h_out + o] = from_f32<T>(yv[u] + acc[u]);
+}
+
 // ---- CUDA-core base GEMM, optional fused expand ---------------------------------------------
 // 64 tokens x 64 outputs per CTA, 256 threads with 4 x 4 outputs each, K-chunks of 16.
 template <typename T>
@@ -508,9 +557,18 @@ static int launch_expand_t(const PoolView& pv, const SegView& sv, const float* s
                            cudaStream_t st) {
     if (sv.n == 0) return LORA_OK;
     T* yp = static_cast<T*>(y);
+    void* args[] = {(void*)&pv, (void*)&sv, (void*)&s_in, (void*)&s_parts, (void*)&yp};
+    if constexpr (sizeof(T) == 2) {
+        // one CTA per (work item, 256 features); items: at most one per LoRA token, and per
+        // segment one partial item beyond n / 4
+        const int items = std::min(sv.n, std::min(sv.n, pv.S) + (sv.n + kItemTok - 1) / kItemTok);
+        const dim3 grid(items, (pv.h_out + 255) / 256);
+        LORA_CUDA_TRY(launch_pdl((const void*)expand_seg_kernel<T>, grid, dim3(256), sizeof(float) * kItemTok * pv.R,
+                                 st, args));
+        return LORA_OK;
+    }
     const dim3 grid((pv.h_out + 255) / 256, (sv.n + kExpTT - 1) / kExpTT);
     const size_t smem = sizeof(float) * kExpTT * pv.R;
-    void* args[] = {(void*)&pv, (void*)&sv, (void*)&s_in, (void*)&s_parts, (void*)&yp};
     LORA_CUDA_TRY(launch_pdl((const void*)expand_kernel<T>, grid, dim3(256), smem, st, args));
     return LORA_OK;
 }

@@ -199,7 +199,11 @@ int lora_linear_fwd_ex(lora_pool_t pool, const void* W_dev, const void* x_dev, v
 int lora_linear_fwd_static_ws(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
                               const lora_segments* seg, int variant, void* stream);
 
-/* Which variant LORA_VARIANT_AUTO picks for n_tokens on this pool (1 or 2). */
+/* Which variant LORA_VARIANT_AUTO picks for n_tokens on this pool (1 or 2): fused, except for
+ * decode batches (<= 256 tokens) whose fused GEMM could not hold every adapter a CTA needs in
+ * shared memory during its main loop (more than 32 tokens per CTA, or more distinct adapters
+ * than it can stage); those run the base GEMM and the segmented expand.  Chosen from GB300
+ * measurements; host-only, no device access. */
 int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant);
 
 /* Message of the last failed call on this host thread ("" if none). */
