@@ -226,6 +226,22 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     float* Rcv = P + (size_t)a.n_pad * BM;
     const bool push = a.push != 0;
 
+    // stage i of this CTA's K walk: its W box and x box, counted on full[i % stages]
+    auto issue_stage = [&](int i) {
+        const int s = i % stages;
+        const int kb = kb0 + ((i + kb_rot) % nkb) * kc;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        if (kc == 1) {
+            tma_load_2d_cta(smem + s * stage_bytes, &tmW, &full[s], kb * BK, m_tile * BM);
+            tma_load_2d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], kb * BK, 0);
+        } else {
+            tma_load_3d_cta(smem + s * stage_bytes, &tmW, &full[s], 0, m_tile * BM, kb);
+            tma_load_3d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], 0, 0, kb);
+        }
+    };
+    // The producer thread initialises the barriers and fills the ring right away, so the first
+    // HBM round trip overlaps the TMEM allocation and the CTA-wide barrier below.
+    const int pre = min(stages, nkb);
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
@@ -236,10 +252,9 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         mbar_init(rbar, 1);
         for (int i = 0; i < 8; ++i) flags[i] = 0;
         fence_barrier_init();
-    }
-    if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
+        for (int i = 0; i < pre; ++i) issue_stage(i);
         prefetch_tmap(&tmY);
         prefetch_tmap(&tmYtail);
     }
@@ -264,19 +279,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // stream releases its dependents only after its own grid-dependency wait.  Only the
         // shrink output (read by the epilogue warps) needs this grid's wait.
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < nkb; ++i) {
+            int issued = pre;  // stages 0 .. pre-1 went out before the CTA-wide barrier
+            for (int i = pre; i < nkb; ++i) {
                 const int s = i % stages;
                 if (i >= stages && !mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, flags)) break;
-                const int kb = kb0 + ((i + kb_rot) % nkb) * kc;
-                mbar_arrive_expect_tx(&full[s], stage_bytes);
-                if (kc == 1) {
-                    tma_load_2d_cta(smem + s * stage_bytes, &tmW, &full[s], kb * BK, m_tile * BM);
-                    tma_load_2d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], kb * BK, 0);
-                } else {
-                    tma_load_3d_cta(smem + s * stage_bytes, &tmW, &full[s], 0, m_tile * BM, kb);
-                    tma_load_3d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], 0, 0, kb);
-                }
+                issue_stage(i);
                 ++issued;
             }
             if (flags[0]) {  // aborted: let copies already in flight land before the CTA exits
