@@ -33,7 +33,7 @@ EXPORTED = (
     "lora_pool_bytes", "lora_pool_create", "lora_pool_destroy", "lora_pool_load_slot", "lora_pool_unload_slot",
     "lora_segment_workspace_bytes", "lora_segment", "lora_segment_status", "lora_linear_workspace_bytes",
     "lora_linear_fwd", "lora_linear_policy", "lora_last_error", "lora_kernel_launch_count",
-    "lora_set_timing_events", "lora_linear_fwd_static_ws", "lora_linear_fwd_ex",
+    "lora_set_timing_events", "lora_linear_fwd_static_ws", "lora_linear_fwd_ex", "lora_pool_load_slots",
 )
 
 
@@ -67,6 +67,7 @@ def _load() -> ctypes.CDLL:
         "lora_pool_destroy": [vp],
         "lora_pool_load_slot": [vp, i32, vp, vp, i32, ctypes.c_float, vp],
         "lora_pool_unload_slot": [vp, i32, vp],
+        "lora_pool_load_slots": [vp, i32, P(i32), P(vp), P(vp), P(i32), P(ctypes.c_float), vp],
         "lora_segment_workspace_bytes": [i32, i32, P(sz)],
         "lora_segment": [vp, i32, vp, vp, sz, P(lora_segments), vp],
         "lora_segment_status": [P(lora_segments), vp, P(i32)],
@@ -153,10 +154,34 @@ def lora_pool_destroy(handle) -> None:
     _check(_lib.lora_pool_destroy(handle))
 
 
+def _dev_or_pinned(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
 def lora_pool_load_slot(handle, slot: int, A: torch.Tensor, B: torch.Tensor, rank: int, alpha: float,
                         stream=None) -> None:
-    _check(_lib.lora_pool_load_slot(handle, slot, _ptr(_dev(A, "A")), _ptr(_dev(B, "B")), rank, float(alpha),
-                                    _stream(stream)))
+    """A and B: device tensors or pinned host tensors (read by the mounting kernel directly)."""
+    _check(_lib.lora_pool_load_slot(handle, slot, _ptr(_dev_or_pinned(A, "A")), _ptr(_dev_or_pinned(B, "B")), rank,
+                                    float(alpha), _stream(stream)))
+
+
+def lora_pool_load_slots(handle, slots, As, Bs, alphas, stream=None) -> None:
+    """Mount len(slots) adapters with one call (As[i], Bs[i]: device or pinned host tensors)."""
+    n = len(slots)
+    if not (len(As) == len(Bs) == len(alphas) == n):
+        raise ValueError("slots, As, Bs and alphas must have the same length")
+    As = [_dev_or_pinned(a, "A") for a in As]
+    Bs = [_dev_or_pinned(b, "B") for b in Bs]
+    arr_i = (ctypes.c_int32 * max(n, 1))
+    arr_p = (ctypes.c_void_p * max(n, 1))
+    arr_f = (ctypes.c_float * max(n, 1))
+    _check(_lib.lora_pool_load_slots(handle, n, arr_i(*[int(s) for s in slots]), arr_p(*[a.data_ptr() for a in As]),
+                                     arr_p(*[b.data_ptr() for b in Bs]), arr_i(*[int(a.shape[0]) for a in As]),
+                                     arr_f(*[float(x) for x in alphas]), _stream(stream)))
 
 
 def lora_pool_unload_slot(handle, slot: int, stream=None) -> None:
@@ -265,6 +290,9 @@ class LoraPool:
 
     def load_slot(self, slot: int, A: torch.Tensor, B: torch.Tensor, alpha: float, stream=None) -> None:
         lora_pool_load_slot(self.handle, slot, A, B, int(A.shape[0]), alpha, stream)
+
+    def load_slots(self, slots, As, Bs, alphas, stream=None) -> None:
+        lora_pool_load_slots(self.handle, slots, As, Bs, alphas, stream)
 
     def unload_slot(self, slot: int, stream=None) -> None:
         lora_pool_unload_slot(self.handle, slot, stream)

@@ -11,6 +11,7 @@
 // default-deny validation of "Multi-LoRA 在线服务隔离" (ai.codenodex.com), section
 // "请求身份决定适配器，而非客户端参数": an unknown or unmounted slot is an explicit error.
 #include <algorithm>
+#include <vector>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -83,6 +84,62 @@ __global__ void pool_load_kernel(const T* __restrict__ A_src, const T* __restric
         entry->rank = r;
         entry->scale = scale;
         entry->state = kSlotReady;
+    }
+}
+
+// ---- batched mount (16-bit pools): up to kLoadBatch slots per launch, 16-byte copies ---------
+constexpr int kLoadBatch = 32;
+struct LoadEntry {
+    const void* A;  // [rank, h_in]
+    const void* B;  // [h_out, rank]
+    int slot, rank;
+    float scale;
+};
+struct LoadBatch {
+    LoadEntry e[kLoadBatch];
+};
+
+// grid (CTAs per slot, slots of the batch).  A slot's A rows and B rows are copied in 16-byte
+// units (8 elements) with the zero padding of rank .. r_max; B rows whose rank is not a
+// multiple of 8 are gathered element by element.  The source may be device memory or host
+// memory the device can read.
+template <typename T>
+__global__ void __launch_bounds__(256)
+pool_load_batch_kernel(const __grid_constant__ LoadBatch b, char* __restrict__ A_base, char* __restrict__ B_base,
+                       SlotEntry* __restrict__ table, int R, int h_in, int h_out) {
+    const LoadEntry& e = b.e[blockIdx.y];
+    uint4* A_dst = reinterpret_cast<uint4*>(A_base + (size_t)e.slot * R * h_in * sizeof(T));
+    uint4* B_dst = reinterpret_cast<uint4*>(B_base + (size_t)e.slot * h_out * R * sizeof(T));
+    const size_t cpr_a = h_in / 8, cpr_b = R / 8;
+    const size_t nA = (size_t)R * cpr_a, nB = (size_t)h_out * cpr_b;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < nA + nB; u += stride) {
+        if (u < nA) {
+            A_dst[u] = u / cpr_a < (size_t)e.rank ? static_cast<const uint4*>(e.A)[u] : zero;
+        } else {
+            const size_t v = u - nA, o = v / cpr_b;
+            const int j0 = (int)(v - o * cpr_b) * 8;
+            uint4 val = zero;
+            if (j0 < e.rank) {
+                const T* src = static_cast<const T*>(e.B) + o * e.rank + j0;
+                if (e.rank % 8 == 0) {
+                    val = *reinterpret_cast<const uint4*>(src);
+                } else {
+                    __align__(16) T tmp[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) tmp[k] = j0 + k < e.rank ? src[k] : T(0.0f);
+                    val = *reinterpret_cast<const uint4*>(tmp);
+                }
+            }
+            B_dst[v] = val;
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        SlotEntry* t = table + e.slot;
+        t->rank = e.rank;
+        t->scale = e.scale;
+        t->state = kSlotReady;
     }
 }
 
@@ -306,25 +363,65 @@ int lora_pool_load_slot(lora_pool_t pool, int slot, const void* A_dev, const voi
     const int blocks = (int)std::min<size_t>((work + threads - 1) / threads, 4096);
     cudaStream_t st = (cudaStream_t)stream;
     SlotEntry* e = static_cast<SlotEntry*>(pool->table) + slot;
-    switch (d.dtype) {
-        case LORA_F32:
-            pool_load_kernel<float><<<blocks, threads, 0, st>>>((const float*)A_dev, (const float*)B_dev,
-                                                                (float*)A_dst, (float*)B_dst, rank, d.r_max,
-                                                                d.h_in, d.h_out, e, scale);
-            break;
-        case LORA_F16:
-            pool_load_kernel<__half><<<blocks, threads, 0, st>>>((const __half*)A_dev, (const __half*)B_dev,
-                                                                 (__half*)A_dst, (__half*)B_dst, rank, d.r_max,
-                                                                 d.h_in, d.h_out, e, scale);
-            break;
-        default:
-            pool_load_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
-                (const __nv_bfloat16*)A_dev, (const __nv_bfloat16*)B_dev, (__nv_bfloat16*)A_dst,
-                (__nv_bfloat16*)B_dst, rank, d.r_max, d.h_in, d.h_out, e, scale);
-    }
+    int r_arg = rank, R_arg = d.r_max, hi = d.h_in, ho = d.h_out;
+    float sc = scale;
+    void* args[] = {(void*)&A_dev, (void*)&B_dev, (void*)&A_dst, (void*)&B_dst, (void*)&r_arg,
+                    (void*)&R_arg, (void*)&hi, (void*)&ho, (void*)&e, (void*)&sc};
+    const void* fn = d.dtype == LORA_F32   ? (const void*)pool_load_kernel<float>
+                     : d.dtype == LORA_F16 ? (const void*)pool_load_kernel<__half>
+                                           : (const void*)pool_load_kernel<__nv_bfloat16>;
+    // the launch's own status (an error left over from earlier work is not reported as ours)
+    LORA_CUDA_TRY(cudaLaunchKernel(fn, dim3(blocks), dim3(threads), args, 0, st));
     count_launch();
-    LORA_CUDA_TRY(cudaGetLastError());
     pool->mounted[slot] = 1;
+    return LORA_OK;
+}
+
+int lora_pool_load_slots(lora_pool_t pool, int count, const int* slots, const void* const* A, const void* const* B,
+                         const int* ranks, const float* alphas, void* stream) {
+    if (!pool) return set_error(LORA_EINVAL, "pool is NULL");
+    if (count < 0) return set_error(LORA_EINVAL, "count < 0");
+    if (count == 0) return LORA_OK;
+    if (!slots || !A || !B || !ranks || !alphas) return set_error(LORA_EINVAL, "slots/A/B/ranks/alphas is NULL");
+    const lora_pool_desc& d = pool->desc;
+    std::vector<char> seen(d.n_slots, 0);
+    bool vec = d.dtype != LORA_F32;
+    for (int i = 0; i < count; ++i) {  // validate everything before anything is enqueued
+        const int slot = slots[i], rank = ranks[i];
+        if (slot < 0 || slot >= d.n_slots) return set_error(LORA_ESLOT, "slot %d outside [0, %d)", slot, d.n_slots);
+        if (rank < 1 || rank > d.r_max) return set_error(LORA_ERANK, "rank %d outside [1, %d]", rank, d.r_max);
+        if (!A[i] || !B[i]) return set_error(LORA_EINVAL, "A/B of entry %d is NULL", i);
+        if (pool->mounted[slot] || seen[slot]) return set_error(LORA_EBUSY, "slot %d already holds an adapter", slot);
+        seen[slot] = 1;
+        if ((reinterpret_cast<uintptr_t>(A[i]) | reinterpret_cast<uintptr_t>(B[i])) % 16) vec = false;
+    }
+    if (!vec) {  // float32 pools or unaligned sources: one mount kernel per slot
+        for (int i = 0; i < count; ++i) {
+            const int rc = lora_pool_load_slot(pool, slots[i], A[i], B[i], ranks[i], alphas[i], stream);
+            if (rc) return rc;
+        }
+        return LORA_OK;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t units = (size_t)d.r_max * (d.h_in / 8) + (size_t)d.h_out * (d.r_max / 8);
+    const int per_slot = (int)std::min<size_t>((units + 255) / 256, 128);
+    const void* fn = d.dtype == LORA_F16 ? (const void*)pool_load_batch_kernel<__half>
+                                         : (const void*)pool_load_batch_kernel<__nv_bfloat16>;
+    for (int c0 = 0; c0 < count; c0 += kLoadBatch) {
+        const int nb = std::min(kLoadBatch, count - c0);
+        LoadBatch b;
+        memset(&b, 0, sizeof(b));
+        for (int i = 0; i < nb; ++i)
+            b.e[i] = LoadEntry{A[c0 + i], B[c0 + i], slots[c0 + i], ranks[c0 + i], alphas[c0 + i] / (float)ranks[c0 + i]};
+        char* Ab = static_cast<char*>(pool->A);
+        char* Bb = static_cast<char*>(pool->B);
+        SlotEntry* tb = static_cast<SlotEntry*>(pool->table);
+        int R = d.r_max, hi = d.h_in, ho = d.h_out;
+        void* args[] = {(void*)&b, (void*)&Ab, (void*)&Bb, (void*)&tb, (void*)&R, (void*)&hi, (void*)&ho};
+        LORA_CUDA_TRY(cudaLaunchKernel(fn, dim3(per_slot, nb), dim3(256), args, 0, st));
+        count_launch();
+        for (int i = 0; i < nb; ++i) pool->mounted[slots[c0 + i]] = 1;
+    }
     return LORA_OK;
 }
 

@@ -133,15 +133,29 @@ int lora_pool_create(const lora_pool_desc* desc, void* dev_mem, size_t bytes, vo
 int lora_pool_destroy(lora_pool_t pool);
 
 /* Mount an adapter into an empty slot: copy A_dev [rank, h_in] and B_dev [h_out, rank]
- * (device pointers, pool dtype, row-major) into the slot with zero padding up to r_max
- * and mark it ready with scale alpha/rank.  Stream-ordered.  Errors: LORA_ESLOT (slot
- * out of range), LORA_ERANK (rank < 1 or > r_max), LORA_EBUSY (slot already mounted:
- * hot swap must unmount first), LORA_EINVAL (null pointers). */
+ * (pool dtype, row-major) into the slot with zero padding up to r_max and mark it ready
+ * with scale alpha/rank.  One kernel, stream-ordered.  A_dev / B_dev may be device memory
+ * or host memory the device can read (pinned host memory under unified addressing; on
+ * GB300 the kernel then reads it over NVLink-C2C, so mounting from host needs no staging
+ * copy); they must stay valid until the kernel has run.  Errors: LORA_ESLOT (slot out of
+ * range), LORA_ERANK (rank < 1 or > r_max), LORA_EBUSY (slot already mounted: hot swap
+ * must unmount first), LORA_EINVAL (null pointers), LORA_ECUDA (launch failed). */
 int lora_pool_load_slot(lora_pool_t pool, int slot, const void* A_dev, const void* B_dev, int rank,
                         float alpha, void* stream);
 
-/* Mark a slot empty again (stream-ordered).  Work already enqueued that reads the slot
- * is unaffected; batches segmented afterwards that name it fail with LORA_EIDX. */
+/* Mount `count` adapters in one go: entry i is (slots[i], A[i], B[i], ranks[i], alphas[i])
+ * with the meaning of lora_pool_load_slot (the arrays are host memory; A[i] / B[i] device
+ * or device-readable host memory).  Every entry is validated before anything is enqueued
+ * (errors as lora_pool_load_slot; a slot named twice is LORA_EBUSY).  16-bit pools with
+ * 16-byte aligned sources mount up to 32 slots per kernel with 16-byte copies. */
+int lora_pool_load_slots(lora_pool_t pool, int count, const int* slots, const void* const* A, const void* const* B,
+                         const int* ranks, const float* alphas, void* stream);
+
+/* Mark a slot empty again (stream-ordered).  Work already enqueued on the same stream that
+ * reads the slot is unaffected (stream order drains it); batches segmented afterwards that
+ * name it fail with LORA_EIDX.  Work on other streams that may still read the slot must be
+ * ordered before a later lora_pool_load_slot into it (an event), since that overwrites the
+ * slot's rows in the order of its own stream. */
 int lora_pool_unload_slot(lora_pool_t pool, int slot, void* stream);
 
 /* ---- segment builder ------------------------------------------------------------------ */

@@ -110,6 +110,49 @@ def test_pool_load_is_exact_zero_pad(lib):
     assert np.array_equal(A, ref.A) and np.array_equal(B, ref.B)
 
 
+def test_pool_load_from_pinned_host_is_identical(lib):
+    # the mounting kernel reads pinned host memory directly (no staging copy): same bytes
+    case = wl.random_case(5, 24, 256, 192, [8, 3, 16], r_max=16, dtype=torch.bfloat16)
+    ad = case.adapters
+    pool_d = make_pool(lib, case)
+    pool_h = lib.LoraPool(case.h_in, case.h_out, ad.r_max, ad.n_slots, case.dtype, DEV)
+    hA = [a.contiguous().pin_memory() for a in ad.A]
+    hB = [b.contiguous().pin_memory() for b in ad.B]
+    for s in range(ad.n_slots):
+        pool_h.load_slot(s, hA[s], hB[s], ad.alphas[s])
+    torch.cuda.synchronize()
+    assert torch.equal(pool_h.mem, pool_d.mem)
+    y, _, _ = run(lib, case, 1, pool=pool_h)
+    assert_parity(y, O.lora_linear_case(case), "linear over a pool mounted from host")
+    with pytest.raises(ValueError):
+        pool_h.load_slot(0, ad.A[0], ad.B[0], ad.alphas[0])  # pageable host memory is refused
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_pool_batched_mount_is_identical(lib, dtype):
+    # one call for every slot (ranks 1..16, some not multiples of 8), from device and from
+    # pinned host memory, byte-identical to one lora_pool_load_slot per slot
+    ranks = [8, 3, 16, 1, 9, 16, 5]
+    case = wl.random_case(6, 8, 264, 136, ranks, r_max=16, dtype=dtype)
+    ad = case.adapters
+    ref = make_pool(lib, case)
+    slots = list(range(ad.n_slots))[::-1]
+    for src in ("device", "host"):
+        pool = lib.LoraPool(case.h_in, case.h_out, ad.r_max, ad.n_slots, case.dtype, DEV)
+        As = [ad.A[s].contiguous() for s in slots]
+        Bs = [ad.B[s].contiguous() for s in slots]
+        As = [a.to(DEV) if src == "device" else a.pin_memory() for a in As]
+        Bs = [b.to(DEV) if src == "device" else b.pin_memory() for b in Bs]
+        pool.load_slots(slots, As, Bs, [ad.alphas[s] for s in slots])
+        torch.cuda.synchronize()
+        assert torch.equal(pool.mem, ref.mem), src
+    with pytest.raises(lib.LoraError) as e:  # a slot named twice: nothing is mounted
+        pool2 = lib.LoraPool(case.h_in, case.h_out, ad.r_max, ad.n_slots, case.dtype, DEV)
+        pool2.load_slots([0, 0], [ad.A[0].to(DEV)] * 2, [ad.B[0].to(DEV)] * 2, [1.0, 1.0])
+    assert e.value.code == lib.LORA_EBUSY
+    pool2.load_slots([0], [ad.A[0].to(DEV)], [ad.B[0].to(DEV)], [1.0])  # slot 0 is still free
+
+
 def test_pool_mount_errors(lib):
     case = wl.random_case(2, 4, 64, 64, [8, 8], r_max=8, dtype=torch.float16)
     pool = make_pool(lib, case)
