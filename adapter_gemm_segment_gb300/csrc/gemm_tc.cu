@@ -543,7 +543,19 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         v[u] = own[q * BM + row];
                         if (use_lsm) v[u] += L_sm[q * BM + row];
                     }
-                    if (push) {
+                    if (push && a.splits == 4) {
+                        // the usual 4-way split: all three peers' partials loaded before any add
+                        float r0[kYBatch], r1[kYBatch], r2[kYBatch];
+#pragma unroll
+                        for (int u = 0; u < kYBatch; ++u) {
+                            const size_t q = (size_t)min(q0 + u, cnt - 1);
+                            r0[u] = Rcv[q * BM + row];
+                            r1[u] = Rcv[((size_t)per + q) * BM + row];
+                            r2[u] = Rcv[((size_t)2 * per + q) * BM + row];
+                        }
+#pragma unroll
+                        for (int u = 0; u < kYBatch; ++u) v[u] += (r0[u] + r1[u]) + r2[u];
+                    } else if (push) {
 #pragma unroll
                         for (int c = 0; c < 7; ++c) {
                             if (c < a.splits - 1) {
