@@ -461,12 +461,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     cluster_sync();  // every CTA of the cluster is past its main loop and has parked its partials
 
     // ---- phase C: send the partial rows of tokens owned by other CTAs ----
-    if (push && threadIdx.x == 64 && flags[1]) {
-        for (int dst = 0; dst < a.splits; ++dst) {
-            if (dst == rank) continue;
-            const int dt0 = dst * per;
-            const int dcnt = max(0, min(n, dt0 + per) - dt0);
-            if (dcnt == 0) continue;
+    if (push && threadIdx.x >= 64 && threadIdx.x < 64 + a.splits && flags[1]) {
+        // one thread per peer, so the copies are issued side by side
+        const int dst = threadIdx.x - 64;
+        const int dt0 = dst * per;
+        const int dcnt = max(0, min(n, dt0 + per) - dt0);
+        if (dst != rank && dcnt > 0) {
             const int slot_idx = rank < dst ? rank : rank - 1;  // sender index in dst's buffer
             const uint32_t dst_addr =
                 mapa_shared(smem_u32(Rcv + (size_t)slot_idx * per * BM), static_cast<uint32_t>(dst));
