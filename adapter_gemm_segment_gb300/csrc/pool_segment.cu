@@ -275,6 +275,8 @@ segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restri
             it[0] = key - 1;
             it[1] = nt;
             for (int u = nt; u < kItemTok; ++u) it[2 + u] = t;  // padding: a valid token
+            it[6] = table[key - 1].rank;                          // the adapter's true rank
+            it[7] = 0;
         }
     }
     pdl_trigger();

@@ -101,6 +101,11 @@ shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* 
     uint4 xv = make_uint4(0, 0, 0, 0);
     if (k0 < k_end) xv = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * h + k0));
     if (s < 0 || status != LORA_OK) return;
+    // rows past the adapter's true rank (only possible with several row groups): A is zero
+    if (gridDim.y > 1 && g * 8 >= pool.table[s].rank) {
+        if (threadIdx.x < 8) s_out[((size_t)ks * seg.n + t) * R + g * 8 + threadIdx.x] = 0.f;
+        return;
+    }
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.f;
@@ -146,7 +151,7 @@ constexpr int kItemTok = 4;  // sorted tokens per work item (built by the segmen
 // shuffles leave lane L the total of sum L).  Output row t (original order) of K part ks:
 // s_out[(ks * n + t) * r_max + row] = scale * partial dot product.
 template <typename T>
-__global__ void __launch_bounds__(128, 5)
+__global__ void __launch_bounds__(128, 4)
 shrink_seg_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
     __shared__ float red[4][32];
     // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
@@ -160,10 +165,18 @@ shrink_seg_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __
     const int status = __ldcg(seg.status);
     const int n_items = __ldcg(seg.nseg + 1);
     const int4 head = __ldcg(reinterpret_cast<const int4*>(seg.items + (size_t)b * 8));      // slot, count, tok0, tok1
-    const int2 tail = __ldcg(reinterpret_cast<const int2*>(seg.items + (size_t)b * 8 + 4));  // tok2, tok3
+    const int4 tail = __ldcg(reinterpret_cast<const int4*>(seg.items + (size_t)b * 8 + 4));  // tok2, tok3, rank
     if (status != LORA_OK || b >= n_items) return;
     const int slot = head.x, nt = head.y;
     const int tok[kItemTok] = {head.z, head.w, tail.x, tail.y};
+    if (g * 8 >= tail.z) {  // rows past the adapter's true rank: A is zero there
+        const int u = threadIdx.x >> 3;
+        if (threadIdx.x < kItemTok * 8 && u < nt) {
+            const int t = u == 0 ? head.z : u == 1 ? head.w : u == 2 ? tail.x : tail.y;
+            s_out[((size_t)ks * seg.n + t) * R + g * 8 + (threadIdx.x & 7)] = 0.f;
+        }
+        return;
+    }
     // this CTA's K range: part ks of gridDim.z, in sweeps of 1024 features (128 threads x 8)
     const int sweeps = ((h + kShrKChunk - 1) / kShrKChunk + gridDim.z - 1) / gridDim.z;
     const int k_beg = ks * sweeps * kShrKChunk;

@@ -98,7 +98,7 @@ typedef struct lora_pool* lora_pool_t;
  *   status_dev        LORA_OK or LORA_EIDX                                    [1]
  *   idx_dev           copy of the batch's idx (original order)               [n]
  *   items_dev         shrink work items: every adapter segment cut into runs of up to 4
- *                     sorted tokens, {slot, count, token[4], 0, 0} each   [n][8]
+ *                     sorted tokens, {slot, count, token[4], rank, 0} each   [n][8]
  * Segments are rebuilt once per batch and reused by every linear layer that runs
  * over that batch, as long as the workspace stays alive and unmodified. */
 typedef struct {

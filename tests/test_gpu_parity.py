@@ -62,7 +62,8 @@ def seg_arrays(ags, seg):
     return {k: v.cpu().numpy() for k, v in ags.segment_arrays(seg).items()}
 
 
-def check_segments(ags, seg, idx, S):
+def check_segments(ags, seg, idx, S, ranks):
+    """ranks[s]: the true rank mounted in slot s (it travels with the shrink work items)."""
     got = seg_arrays(ags, seg)
     perm, ss, sl, nseg = O.segments(np.asarray(idx), S)
     assert int(got["status"][0]) == 0
@@ -79,10 +80,10 @@ def check_segments(ags, seg, idx, S):
             continue
         for j0 in range(ss[i], ss[i + 1], 4):
             toks = [int(t) for t in perm[j0:min(j0 + 4, ss[i + 1])]]
-            want.append([int(sl[i]), len(toks)] + toks + [toks[0]] * (4 - len(toks)))
+            want.append([int(sl[i]), len(toks)] + toks + [toks[0]] * (4 - len(toks)) + [int(ranks[sl[i]])])
     assert int(got["nseg"][1]) == len(want)
-    items = got["items"].reshape(-1, 8)[:len(want), :6]
-    assert np.array_equal(items, np.array(want, dtype=np.int32).reshape(-1, 6))
+    items = got["items"].reshape(-1, 8)[:len(want), :7]
+    assert np.array_equal(items, np.array(want, dtype=np.int32).reshape(-1, 7))
 
 
 # ------------------------------------------------------------------------------------------
@@ -199,7 +200,7 @@ def test_segments_bitexact(lib, name):
         pool.load_slot(s, A, B, 8.0)
     seg = pool.segment(torch.from_numpy(idx).to(DEV))
     torch.cuda.synchronize()
-    check_segments(lib, seg, idx, S)
+    check_segments(lib, seg, idx, S, [8] * S)
 
 
 def test_segments_empty_batch(lib):
@@ -238,7 +239,7 @@ def test_tiny_fp32(lib, variant):
     case = wl.tiny()
     y, pool, seg = run(lib, case, variant)
     torch.cuda.synchronize()
-    check_segments(lib, seg, case.idx.numpy(), 4)
+    check_segments(lib, seg, case.idx.numpy(), 4, case.adapters.ranks)
     assert_parity(y, O.lora_linear_case(case), f"tiny variant {variant}")
     y0, _, _ = run(lib, case, variant, W=torch.zeros_like(case.W))
     pool0 = O.pool_of_case(case)
@@ -271,7 +272,7 @@ def test_small_cases(lib, spec, variant):
     seed, n, h_in, h_out, ranks, r_max, dtype = spec
     case = wl.random_case(seed, n, h_in, h_out, ranks, r_max=r_max, dtype=dtype, p_base=0.15)
     y, pool, seg = run(lib, case, variant)
-    check_segments(lib, seg, case.idx.numpy(), len(ranks))
+    check_segments(lib, seg, case.idx.numpy(), len(ranks), ranks)
     assert_parity(y, O.lora_linear_case(case), f"{case.name} variant {variant}")
     y0, _, _ = run(lib, case, variant, W=torch.zeros_like(case.W), pool=pool)
     assert_lora_only_parity(y0, O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case),
@@ -313,7 +314,7 @@ def test_repeated_calls_are_bit_identical(lib):
 def test_decode_q_proj_full(lib, variant):
     case = wl.decode_q_proj()
     y, pool, seg = run(lib, case, variant)
-    check_segments(lib, seg, case.idx.numpy(), 100)
+    check_segments(lib, seg, case.idx.numpy(), 100, case.adapters.ranks)
     y_ref = O.lora_linear_case(case)
     assert_parity(y, y_ref, f"decode q_proj variant {variant}")
     y0, _, _ = run(lib, case, variant, W=torch.zeros_like(case.W), pool=pool)
@@ -345,7 +346,7 @@ def test_prefill_full_sampled(lib):
         for variant in (1, 2):
             y, pool, seg = run(lib, case, variant)
             if variant == 1:
-                check_segments(lib, seg, case.idx.numpy(), 100)
+                check_segments(lib, seg, case.idx.numpy(), 100, case.adapters.ranks)
             assert_parity(y[rows], O.lora_linear_case(case, rows=rows), f"{case.name} variant {variant}")
         y0, _, _ = run(lib, case, 1, W=torch.zeros_like(case.W), pool=pool)
         y0_ref = O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case), case.idx.numpy(), rows=rows)
