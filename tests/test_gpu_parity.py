@@ -263,6 +263,9 @@ SMALL = [
     (21, 40, 704, 136, [8, 16, 16], 16, torch.float16),
     # r_max 64 at 100 tokens: the segmented shrink (4-token items), ragged K (4104 features)
     (22, 100, 4104, 64, [64, 8, 16, 64, 1], 64, torch.bfloat16),
+    # the limits of the pool: the largest rank (256) and the most slots (2048)
+    (23, 40, 512, 264, [256, 100, 8, 33], 256, torch.float16),
+    (24, 100, 64, 72, [8] * 2048, 8, torch.float16),
 ]
 
 
