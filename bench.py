@@ -330,8 +330,8 @@ def read_profile_traffic(kernel_key):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     fields = {}
     for line in open(path):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
+        if ": " in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(": ", 1)  # keys contain ':' (sha256[:16])
             fields[k.strip()] = v.strip()
     if fields.get("gemm_tc.cu sha256[:16]") != sha:
         return None
