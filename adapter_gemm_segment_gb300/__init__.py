@@ -34,6 +34,7 @@ EXPORTED = (
     "lora_segment_workspace_bytes", "lora_segment", "lora_segment_status", "lora_linear_workspace_bytes",
     "lora_linear_fwd", "lora_linear_policy", "lora_last_error", "lora_kernel_launch_count",
     "lora_set_timing_events", "lora_linear_fwd_static_ws", "lora_linear_fwd_ex", "lora_pool_load_slots",
+    "lora_linear_group_workspace_bytes", "lora_linear_fwd_group", "lora_linear_group_policy",
 )
 
 
@@ -77,6 +78,9 @@ def _load() -> ctypes.CDLL:
         "lora_set_timing_events": [vp, vp, vp],
         "lora_linear_fwd_static_ws": [vp, vp, vp, vp, P(lora_segments), i32, vp],
         "lora_linear_fwd_ex": [vp, vp, vp, vp, P(lora_segments), i32, vp, sz, vp, sz, vp],
+        "lora_linear_group_workspace_bytes": [i32, P(vp), i32, P(sz)],
+        "lora_linear_fwd_group": [i32, P(vp), vp, vp, vp, P(lora_segments), i32, vp, sz, vp],
+        "lora_linear_group_policy": [i32, P(vp), i32, P(i32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -250,6 +254,38 @@ def lora_linear_fwd(pool_handle, W: torch.Tensor, x: torch.Tensor, y: torch.Tens
     _check(_lib.lora_linear_fwd(pool_handle, _ptr(_dev(W, "W")), _ptr(_dev(x, "x")), _ptr(_dev(y, "y")),
                                 ctypes.byref(seg), variant, _ptr(_dev(ws, "ws")), ws.numel() * ws.element_size(),
                                 _stream(stream)))
+    return y
+
+
+def _handles(pool_handles) -> tuple:
+    hs = list(pool_handles)
+    arr = (ctypes.c_void_p * max(1, len(hs)))(*[h.value if isinstance(h, ctypes.c_void_p) else h for h in hs])
+    return len(hs), arr
+
+
+def lora_linear_group_workspace_bytes(pool_handles, n_tokens: int) -> int:
+    count, arr = _handles(pool_handles)
+    out = ctypes.c_size_t()
+    _check(_lib.lora_linear_group_workspace_bytes(count, arr, n_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def lora_linear_group_policy(pool_handles, n_tokens: int) -> int:
+    count, arr = _handles(pool_handles)
+    out = ctypes.c_int()
+    _check(_lib.lora_linear_group_policy(count, arr, n_tokens, ctypes.byref(out)))
+    return out.value
+
+
+def lora_linear_fwd_group(pool_handles, W: torch.Tensor, x: torch.Tensor, y: torch.Tensor, seg: lora_segments,
+                          ws: torch.Tensor, variant: int = LORA_VARIANT_AUTO, stream=None) -> torch.Tensor:
+    """Projections sharing x and segments as one linear: W [sum h_out_q, h_in] (slices stacked
+    row-wise, slice q's adapters in pool_handles[q]), y [n, sum h_out_q] (slice q = its column
+    range)."""
+    count, arr = _handles(pool_handles)
+    _check(_lib.lora_linear_fwd_group(count, arr, _ptr(_dev(W, "W")), _ptr(_dev(x, "x")), _ptr(_dev(y, "y")),
+                                      ctypes.byref(seg), variant, _ptr(_dev(ws, "ws")),
+                                      ws.numel() * ws.element_size(), _stream(stream)))
     return y
 
 

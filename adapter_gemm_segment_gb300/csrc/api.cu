@@ -187,3 +187,154 @@ int lora_linear_fwd_ex(lora_pool_t pool, const void* W_dev, const void* x_dev, v
 }
 
 }  // extern "C"
+
+// ---- grouped projections ------------------------------------------------------------------
+
+namespace lora {
+
+// Checks the pools of a group and builds the pool views and the slice table (s_stride left 0).
+static int group_setup(int count, const lora_pool_t* pools, PoolView* pvs, GroupView* grp) {
+    if (count < 1 || count > kMaxGroup) return set_error(LORA_EINVAL, "group of %d slices (1..%d)", count, kMaxGroup);
+    if (!pools) return set_error(LORA_EINVAL, "pools is NULL");
+    for (int q = 0; q < count; ++q) {
+        if (!pools[q]) return set_error(LORA_EINVAL, "pools[%d] is NULL", q);
+        pvs[q] = pool_view(pools[q]);
+    }
+    const PoolView& p0 = pvs[0];
+    if (p0.dtype != LORA_F16 && p0.dtype != LORA_BF16)
+        return set_error(LORA_EUNSUP, "grouped projections need fp16 or bf16 pools");
+    memset(grp, 0, sizeof(*grp));
+    grp->count = count;
+    for (int q = 0; q < count; ++q) {
+        const PoolView& p = pvs[q];
+        if (p.h_in != p0.h_in || p.R != p0.R || p.S != p0.S || p.dtype != p0.dtype)
+            return set_error(LORA_EINVAL, "pool %d differs from pool 0 in h_in, r_max, n_slots or dtype", q);
+        if (count > 1 && p.h_out % 16)
+            return set_error(LORA_EINVAL, "pool %d: h_out %d is not a multiple of 16", q, p.h_out);
+        if (pools[q]->mounted != pools[0]->mounted)
+            return set_error(LORA_EINVAL, "pool %d does not hold the same slots as pool 0", q);
+        grp->table[q] = p.table;
+        grp->A[q] = p.A;
+        grp->B[q] = p.B;
+        grp->col[q + 1] = grp->col[q] + p.h_out;
+        grp->blk[q + 1] = grp->blk[q] + (p.h_out + 255) / 256;
+    }
+    grp->ldy = grp->col[count];
+    return LORA_OK;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+int lora_linear_group_workspace_bytes(int count, const lora_pool_t* pools, int n_tokens, size_t* bytes) {
+    if (!bytes) return set_error(LORA_EINVAL, "bytes is NULL");
+    if (n_tokens < 0) return set_error(LORA_EINVAL, "n_tokens < 0");
+    PoolView pvs[kMaxGroup];
+    GroupView grp;
+    const int rc = group_setup(count, pools, pvs, &grp);
+    if (rc) return rc;
+    *bytes = (size_t)count * lin_layout(pvs[0], n_tokens).total;
+    return LORA_OK;
+}
+
+int lora_linear_group_policy(int count, const lora_pool_t* pools, int n_tokens, int* variant) {
+    if (!variant) return set_error(LORA_EINVAL, "variant is NULL");
+    PoolView pvs[kMaxGroup];
+    GroupView grp;
+    const int rc = group_setup(count, pools, pvs, &grp);
+    if (rc) return rc;
+    // Measured on GB300 (7B-shaped layers, 64 and 256 tokens, bf16, r_max 16): the base GEMM
+    // over the concatenated weight plus one segmented expand beat per-slice fused GEMMs at
+    // decode sizes; prefill batches keep the fused epilogue.
+    *variant = n_tokens <= 256 ? LORA_VARIANT_SEPARATE : LORA_VARIANT_FUSED;
+    return LORA_OK;
+}
+
+int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev, const void* x_dev, void* y_dev,
+                          const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes, void* stream) {
+    if (!seg) return set_error(LORA_EINVAL, "seg is NULL");
+    PoolView pvs[kMaxGroup];
+    GroupView grp;
+    int rc = group_setup(count, pools, pvs, &grp);
+    if (rc) return rc;
+    const PoolView& p0 = pvs[0];
+    const int n = seg->n_tokens;
+    if (seg->n_slots != p0.S)
+        return set_error(LORA_EINVAL, "segments were built for %d slots, pools have %d", seg->n_slots, p0.S);
+    if (variant != LORA_VARIANT_AUTO && variant != LORA_VARIANT_FUSED && variant != LORA_VARIANT_SEPARATE)
+        return set_error(variant == kVariantCudaCore ? LORA_EUNSUP : LORA_EINVAL, "variant %d for a group", variant);
+    if (n == 0) return LORA_OK;
+    if (!W_dev || !x_dev || !y_dev || !ws_dev) return set_error(LORA_EINVAL, "W/x/y/ws is NULL");
+    if ((reinterpret_cast<uintptr_t>(W_dev) | reinterpret_cast<uintptr_t>(x_dev) | reinterpret_cast<uintptr_t>(y_dev)) %
+        16)
+        return set_error(LORA_EINVAL, "W/x/y must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(ws_dev) % 256) return set_error(LORA_EINVAL, "ws must be 256-byte aligned");
+    const size_t slice_ws = lin_layout(p0, n).total;
+    if (ws_bytes < (size_t)count * slice_ws)
+        return set_error(LORA_ENOSPACE, "group workspace needs %zu bytes, got %zu", (size_t)count * slice_ws, ws_bytes);
+    grp.s_stride = (long long)(slice_ws / sizeof(float));
+    PoolView pcat = p0;  // the concatenated linear: [sum of h_out, h_in]
+    pcat.h_out = grp.ldy;
+    if (!tc_supported(pcat, n)) return set_error(LORA_EUNSUP, "no tensor-core plan for this group and batch");
+    if (variant == LORA_VARIANT_AUTO) lora_linear_group_policy(count, pools, n, &variant);
+    const bool fused = variant == LORA_VARIANT_FUSED;
+    const bool decode = n <= 256;
+    if (decode && fused)
+        for (int q = 0; q < count; ++q)
+            if (!tc_supported(pvs[q], n)) return set_error(LORA_EUNSUP, "no fused tensor-core plan for slice %d", q);
+    const SegView sv = seg_view(seg);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* s_buf = static_cast<float*>(ws_dev);
+    const size_t elt = dtype_size(p0.dtype);
+
+    record_if(g_ev_before_shrink, st);
+    int s_parts = 1;
+    if (decode) {
+        rc = launch_shrink_group(p0, grp, sv, x_dev, s_buf, st, /*tiled=*/false, &s_parts);  // every slice, one launch
+        if (rc) return rc;
+    } else {
+        for (int q = 0; q < count; ++q) {
+            float* s_q = s_buf + (size_t)q * grp.s_stride;
+            rc = shrink_tc_supported(pvs[q]) ? launch_shrink_tc(pvs[q], sv, x_dev, s_q, st)
+                                             : launch_shrink(pvs[q], sv, x_dev, s_q, st, /*tiled=*/true, &s_parts);
+            if (rc) return rc;
+        }
+    }
+    record_if(g_ev_before_gemm, st);
+    if (decode && fused) {
+        // the decode kernel's fused epilogue serves one pool: one launch per slice, each writing
+        // its column range of y
+        for (int q = 0; q < count; ++q) {
+            GroupView gq;
+            memset(&gq, 0, sizeof(gq));
+            gq.count = 1;
+            gq.ldy = grp.ldy;
+            gq.col[1] = pvs[q].h_out;
+            gq.blk[1] = (pvs[q].h_out + 255) / 256;
+            gq.table[0] = pvs[q].table;
+            gq.A[0] = pvs[q].A;
+            gq.B[0] = pvs[q].B;
+            const char* Wq = static_cast<const char*>(W_dev) + (size_t)grp.col[q] * p0.h_in * elt;
+            char* yq = static_cast<char*>(y_dev) + (size_t)grp.col[q] * elt;
+            rc = launch_gemm_tc(pvs[q], sv, Wq, x_dev, s_buf + (size_t)q * grp.s_stride, s_parts, yq, true, st, nullptr,
+                                0, &gq);
+            if (rc) return rc;
+        }
+    } else {
+        // one base GEMM over the concatenated weight; the prefill kernel applies each slice's
+        // LoRA term in its epilogue
+        rc = launch_gemm_tc(pcat, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused && !decode, st, nullptr, 0, &grp);
+        if (rc) return rc;
+    }
+    record_if(g_ev_after_gemm, st);
+    if (!fused) {
+        rc = launch_expand_group(p0, grp, sv, s_buf, s_parts, y_dev, st);
+        if (rc) return rc;
+    }
+    return LORA_OK;
+}
+
+}  // extern "C"

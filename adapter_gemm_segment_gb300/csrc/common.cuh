@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <vector>
 
@@ -69,6 +70,63 @@ inline SegView seg_view(const lora_segments* s) {
     v.items = s->items_dev;
     v.n = s->n_tokens;
     return v;
+}
+
+// Projections that read the same x and the same segments (q, k and v of an attention block;
+// gate and up of an MLP) run as one linear over their row-concatenated base weight.  Slice q
+// owns output columns [col[q], col[q + 1]) of y, whose row stride is ldy = col[count], and
+// has its own adapter pool (same h_in, r_max, slot count and dtype as the others).  A single
+// linear is the one-slice case.
+constexpr int kMaxGroup = 4;
+struct GroupView {
+    int count;
+    int ldy;
+    int col[kMaxGroup + 1];
+    int blk[kMaxGroup + 1];  // first 256-feature block of each slice (segmented expand grid)
+    const SlotEntry* table[kMaxGroup];
+    const void* A[kMaxGroup];
+    const void* B[kMaxGroup];
+    long long s_stride;  // floats between the shrink outputs of consecutive slices
+};
+
+inline GroupView single_group(const PoolView& pv) {
+    GroupView g;
+    memset(&g, 0, sizeof(g));
+    g.count = 1;
+    g.ldy = pv.h_out;
+    g.col[1] = pv.h_out;
+    g.blk[1] = (pv.h_out + 255) / 256;
+    g.table[0] = pv.table;
+    g.A[0] = pv.A;
+    g.B[0] = pv.B;
+    return g;
+}
+
+// One slice of a group, selected with compile-time indices (no local-memory copy of the
+// parameter block).
+struct SliceRef {
+    const SlotEntry* table;
+    const void* A;
+    const void* B;
+    int col, h_out;
+    long long s_off;
+};
+
+__device__ __forceinline__ SliceRef group_slice(const GroupView& g, int q) {
+    SliceRef r{g.table[0], g.A[0], g.B[0], g.col[0], g.col[1] - g.col[0], 0};
+#pragma unroll
+    for (int i = 1; i < kMaxGroup; ++i)
+        if (i == q) r = SliceRef{g.table[i], g.A[i], g.B[i], g.col[i], g.col[i + 1] - g.col[i], i * g.s_stride};
+    return r;
+}
+
+// Slice owning output column c (columns of one slice are contiguous).
+__device__ __forceinline__ int group_slice_of_col(const GroupView& g, int c) {
+    int q = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxGroup; ++i)
+        if (i < g.count && c >= g.col[i]) q = i;
+    return q;
 }
 
 inline size_t dtype_size(int dt) { return dt == LORA_F32 ? 4 : 2; }

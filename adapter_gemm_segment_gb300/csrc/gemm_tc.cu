@@ -64,6 +64,7 @@ struct DecodeArgs {
 
 struct PrefillArgs {
     PoolView pool;
+    GroupView grp;  // output slices (one for a single linear); y row stride grp.ldy
     SegView seg;
     const float* s_in;
     void* y;
@@ -730,8 +731,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     } else {
         // ---- epilogue: thread <-> token row (TMEM lane), 256 features per tile ----
         const int q = warp & 3;
-        const int h_out = a.pool.h_out, R = a.pool.R, n = a.n;
-        const T* B = static_cast<const T*>(a.pool.B);
+        const int ldy = a.grp.ldy, R = a.pool.R, n = a.n;
         T* y = static_cast<T*>(a.y);
         bool waited = false;
         int status = LORA_OK;
@@ -751,19 +751,22 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const int t = m0 + q * 32 + lane;
             const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
             const int slot = (a.fuse && t < n) ? __ldcg(a.seg.idx + t) : -1;
-            const float* srow = a.s_in + (size_t)(t < n ? t : 0) * R;
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 uint32_t r[16];
                 __syncwarp();
                 tmem_ld16(taddr + c0, r);
                 tmem_ld_wait();
-                if (status != LORA_OK || t >= n || n0 + c0 >= h_out) continue;  // after the warp-wide load
+                const int col = n0 + c0;  // column of y
+                if (status != LORA_OK || t >= n || col >= ldy) continue;  // after the warp-wide load
                 float v[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
                 if (slot >= 0) {
-                    const T* Bt = B + ((size_t)slot * h_out + n0 + c0) * R;
-                    const int cmax = min(16, h_out - (n0 + c0));
+                    // the slice owning these 16 columns (slice boundaries are multiples of 16)
+                    const SliceRef sl = group_slice(a.grp, group_slice_of_col(a.grp, col));
+                    const float* srow = a.s_in + sl.s_off + (size_t)t * R;
+                    const T* Bt = static_cast<const T*>(sl.B) + ((size_t)slot * sl.h_out + (col - sl.col)) * R;
+                    const int cmax = min(16, sl.col + sl.h_out - col);
                     for (int j0 = 0; j0 < R; j0 += 8) {
                         const float4 sa = __ldg(reinterpret_cast<const float4*>(srow + j0));
                         const float4 sb = __ldg(reinterpret_cast<const float4*>(srow + j0 + 4));
@@ -789,11 +792,11 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         }
                     }
                 }
-                T* yp = y + (size_t)t * h_out + n0 + c0;
+                T* yp = y + (size_t)t * ldy + col;
                 alignas(16) T outv[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) outv[c] = from_f32<T>(v[c]);
-                if (n0 + c0 + 16 <= h_out) {
+                if (col + 16 <= ldy) {
                     reinterpret_cast<uint4*>(yp)[0] = reinterpret_cast<const uint4*>(outv)[0];
                     reinterpret_cast<uint4*>(yp)[1] = reinterpret_cast<const uint4*>(outv)[1];
                 } else {  // h_out is a multiple of 8: one half-chunk remains
@@ -903,12 +906,18 @@ int decode_fused_fits(const PoolView& pv, int n) {
 
 template <typename T>
 static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
-                       int s_parts, void* y, bool fuse, const void* prefetch, size_t prefetch_bytes, cudaStream_t st) {
+                       int s_parts, void* y, bool fuse, const void* prefetch, size_t prefetch_bytes,
+                       const GroupView* grp, cudaStream_t st) {
     using namespace tc;
     const int n = sv.n;
     if (n == 0) return LORA_OK;
     const int bf16 = pv.dtype == LORA_BF16;
+    const GroupView g1 = grp ? *grp : single_group(pv);
+    if (g1.ldy < pv.h_out) return set_error(LORA_EINVAL, "internal: y row stride below h_out");
     if (n <= kDecodeMaxN) {
+        // the decode kernel's LoRA epilogue knows one pool: a group runs it per slice, or its
+        // base GEMM over the concatenated weight without the LoRA term
+        if (g1.count != 1 && fuse) return set_error(LORA_EINVAL, "internal: fused decode GEMM of several slices");
         const DecodePlan p = plan_decode(pv, n, s_parts);
         CUtensorMap mW, mX, mY;
         int rc;
@@ -926,9 +935,9 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         const int ychunk = std::min(kYChunk, per);
         const int ytail = per % ychunk;
         CUtensorMap mYt;
-        rc = make_map_plain(&mY, y, bf16, pv.h_out, n, BM, ychunk);
+        rc = make_map_plain(&mY, y, bf16, pv.h_out, n, BM, ychunk, g1.ldy);
         if (rc) return rc;
-        rc = make_map_plain(&mYt, y, bf16, pv.h_out, n, BM, ytail ? ytail : ychunk);
+        rc = make_map_plain(&mYt, y, bf16, pv.h_out, n, BM, ytail ? ytail : ychunk, g1.ldy);
         if (rc) return rc;
         DecodeArgs a;
         a.pool = pv;
@@ -979,8 +988,10 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     }
     // prefill
     if (s_parts != 1) return set_error(LORA_EINVAL, "internal: prefill GEMM expects an unsplit shrink output");
+    if (g1.col[g1.count] != pv.h_out) return set_error(LORA_EINVAL, "internal: slices do not cover h_out");
     PrefillArgs a;
     a.pool = pv;
+    a.grp = g1;
     a.seg = sv;
     a.s_in = s_in;
     a.y = y;
@@ -1012,10 +1023,11 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
 }
 
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
-                   void* y, bool fuse, cudaStream_t st, const void* prefetch, size_t prefetch_bytes) {
+                   void* y, bool fuse, cudaStream_t st, const void* prefetch, size_t prefetch_bytes,
+                   const GroupView* grp) {
     if (pv.dtype == LORA_F16)
-        return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, st);
-    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, st);
+        return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st);
+    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st);
 }
 
 }  // namespace lora

@@ -14,6 +14,10 @@ namespace lora {
 int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled,
                   int* s_parts);
 int shrink_parts(const PoolView& pv, int n, bool tiled);
+// The same for the slices of a group (16-bit data, not tiled): slice q's output starts at
+// s_out + q * grp.s_stride.  One launch covers every slice.
+int launch_shrink_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,
+                        cudaStream_t st, bool tiled, int* s_parts);
 
 // Whether the fused tensor-core decode GEMM (n <= 256) holds every adapter's B rows a CTA can
 // need in shared memory during its main loop (the variant policy keys on this).
@@ -21,6 +25,10 @@ int decode_fused_fits(const PoolView& pv, int n);
 
 // y[t, :] += s[t, :] B_s^T (separate variant's residual kernel).
 int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, int s_parts, void* y, cudaStream_t st);
+// The same for the slices of a group (16-bit data): y has row stride grp.ldy, slice q owns
+// columns [grp.col[q], grp.col[q + 1]).  One launch covers every slice.
+int launch_expand_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const float* s_in, int s_parts,
+                        void* y, cudaStream_t st);
 
 // CUDA-core base GEMM y = x W^T (+ fused expand when fuse).
 int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
@@ -33,8 +41,13 @@ int launch_gemm_simt(const PoolView& pv, const SegView& sv, const void* W, const
 int tc_supported(const PoolView& pv, int n);
 // prefetch/prefetch_bytes: optional device range the decode kernel streams into L2 after its
 // own loads (ignored by the prefill kernel).
+// grp: output slices of a group (nullptr: the single linear of pv).  pv.h_out is then the
+// concatenated width; y has row stride grp->ldy.  The prefill kernel applies every slice's
+// LoRA term; the decode kernel takes one slice with fuse, or several without the LoRA term
+// (a single slice may also be a column range of a wider y: pv.h_out < grp->ldy).
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
-                   void* y, bool fuse, cudaStream_t st, const void* prefetch = nullptr, size_t prefetch_bytes = 0);
+                   void* y, bool fuse, cudaStream_t st, const void* prefetch = nullptr, size_t prefetch_bytes = 0,
+                   const GroupView* grp = nullptr);
 
 // Grouped tcgen05 shrink for batches of more than 256 tokens (one CTA per 128-token tile).
 int shrink_tc_supported(const PoolView& pv);

@@ -82,14 +82,18 @@ constexpr int kShrKChunk = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(128)
-shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
+shrink_token_kernel(PoolView pool, GroupView grp, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
     __shared__ float red[4][8];
     // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
     // every kernel before this one has completed (x, W) and waits separately for s.
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.x, g = blockIdx.y, ks = blockIdx.z;
-    const int h = pool.h_in, R = pool.R;
+    const int t = blockIdx.x, ks = blockIdx.z;
+    const int h = pool.h_in, R = pool.R, rg = R / 8;
+    // grid rows: (slice of the group, 8-row group of r_max)
+    const int qs = blockIdx.y / rg, g = blockIdx.y - qs * rg;
+    const SliceRef sl = group_slice(grp, qs);
+    s_out += sl.s_off;
     // this CTA's K range: part ks of gridDim.z, in sweeps of 1024 features (128 threads x 8)
     const int sweeps = ((h + kShrKChunk - 1) / kShrKChunk + gridDim.z - 1) / gridDim.z;
     const int k_beg = ks * sweeps * kShrKChunk;
@@ -102,14 +106,14 @@ shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* 
     if (k0 < k_end) xv = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * h + k0));
     if (s < 0 || status != LORA_OK) return;
     // rows past the adapter's true rank (only possible with several row groups): A is zero
-    if (gridDim.y > 1 && g * 8 >= pool.table[s].rank) {
+    if (rg > 1 && g * 8 >= sl.table[s].rank) {
         if (threadIdx.x < 8) s_out[((size_t)ks * seg.n + t) * R + g * 8 + threadIdx.x] = 0.f;
         return;
     }
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.f;
-    const T* Ab = static_cast<const T*>(pool.A) + ((size_t)s * R + (size_t)g * 8) * h;
+    const T* Ab = static_cast<const T*>(sl.A) + ((size_t)s * R + (size_t)g * 8) * h;
     for (int k = k0; k < k_end; k += kShrKChunk) {
         if (k != k0) xv = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)t * h + k));
         uint4 av[8];
@@ -125,7 +129,7 @@ shrink_token_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* 
             for (int e = 0; e < 8; ++e) acc[r] = fmaf(xf[e], af[e], acc[r]);
         }
     }
-    const float scale = pool.table[s].scale;
+    const float scale = sl.table[s].scale;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -152,14 +156,18 @@ constexpr int kItemTok = 4;  // sorted tokens per work item (built by the segmen
 // s_out[(ks * n + t) * r_max + row] = scale * partial dot product.
 template <typename T>
 __global__ void __launch_bounds__(128, 4)
-shrink_seg_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
+shrink_seg_kernel(PoolView pool, GroupView grp, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
     __shared__ float red[4][32];
     // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
     // every kernel before this one has completed (x, W) and waits separately for s.
     pdl_wait();
     pdl_trigger();
-    const int b = blockIdx.x, g = blockIdx.y, ks = blockIdx.z;
-    const int h = pool.h_in, R = pool.R;
+    const int b = blockIdx.x, ks = blockIdx.z;
+    const int h = pool.h_in, R = pool.R, rg = R / 8;
+    // grid rows: (slice of the group, 8-row group of r_max)
+    const int qs = blockIdx.y / rg, g = blockIdx.y - qs * rg;
+    const SliceRef sl = group_slice(grp, qs);
+    s_out += sl.s_off;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // independent loads first: status, item count, the item
     const int status = __ldcg(seg.status);
@@ -169,7 +177,10 @@ shrink_seg_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __
     if (status != LORA_OK || b >= n_items) return;
     const int slot = head.x, nt = head.y;
     const int tok[kItemTok] = {head.z, head.w, tail.x, tail.y};
-    if (g * 8 >= tail.z) {  // rows past the adapter's true rank: A is zero there
+    // Rows past the adapter's true rank: A is zero there.  The item carries the rank in the
+    // pool the segments were built on; segments may be shared by pools with the same slot
+    // count, and this pool may hold the slot at a larger rank, so its own table decides.
+    if (g * 8 >= tail.z && g * 8 >= sl.table[slot].rank) {
         const int u = threadIdx.x >> 3;
         if (threadIdx.x < kItemTok * 8 && u < nt) {
             const int t = u == 0 ? head.z : u == 1 ? head.w : u == 2 ? tail.x : tail.y;
@@ -181,7 +192,7 @@ shrink_seg_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __
     const int sweeps = ((h + kShrKChunk - 1) / kShrKChunk + gridDim.z - 1) / gridDim.z;
     const int k_beg = ks * sweeps * kShrKChunk;
     const int k_end = min(h, k_beg + sweeps * kShrKChunk);
-    const T* Ab = static_cast<const T*>(pool.A) + ((size_t)slot * R + (size_t)g * 8) * h;
+    const T* Ab = static_cast<const T*>(sl.A) + ((size_t)slot * R + (size_t)g * 8) * h;
     float v[kItemTok * 8];  // v[u * 8 + r]: token u, adapter row g*8 + r
 #pragma unroll
     for (int e = 0; e < kItemTok * 8; ++e) v[e] = 0.f;
@@ -223,7 +234,7 @@ shrink_seg_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* __
         if (u < nt) {
             const float sum = red[0][threadIdx.x] + red[1][threadIdx.x] + red[2][threadIdx.x] + red[3][threadIdx.x];
             const int t = u == 0 ? head.z : u == 1 ? head.w : u == 2 ? tail.x : tail.y;
-            s_out[((size_t)ks * seg.n + t) * R + g * 8 + r] = pool.table[slot].scale * sum;
+            s_out[((size_t)ks * seg.n + t) * R + g * 8 + r] = sl.table[slot].scale * sum;
         }
     }
 }
@@ -388,33 +399,46 @@ expand_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, int s_
 // adds the LoRA term of every token of the item.
 template <typename T>
 __global__ void __launch_bounds__(256)
-expand_seg_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, int s_parts, T* __restrict__ y) {
+expand_seg_kernel(PoolView pool, GroupView grp, SegView seg, const float* __restrict__ s_in, int s_parts,
+                  T* __restrict__ y) {
     extern __shared__ float ss[];  // [4][R]: the item's shrink rows (K parts summed)
     pdl_wait();
     pdl_trigger();
     const int b = blockIdx.x;
+    // grid columns: 256-feature blocks of the group's slices, one after another
+    int qs = 0, blk0 = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxGroup; ++i)
+        if (i < grp.count && (int)blockIdx.y >= grp.blk[i]) {
+            qs = i;
+            blk0 = grp.blk[i];
+        }
+    const SliceRef sl = group_slice(grp, qs);
+    s_in += sl.s_off;
     const int status = __ldcg(seg.status);
     const int n_items = __ldcg(seg.nseg + 1);
     const int4 head = __ldcg(reinterpret_cast<const int4*>(seg.items + (size_t)b * 8));      // slot, count, tok0, tok1
     const int2 tail = __ldcg(reinterpret_cast<const int2*>(seg.items + (size_t)b * 8 + 4));  // tok2, tok3
     if (status != LORA_OK || b >= n_items) return;
-    const int R = pool.R, h_out = pool.h_out, slot = head.x, nt = head.y;
+    const int R = pool.R, h_out = sl.h_out, ldy = grp.ldy, slot = head.x, nt = head.y;
     const int tok[kItemTok] = {head.z, head.w, tail.x, tail.y};
     for (int e = threadIdx.x; e < kItemTok * R; e += blockDim.x) {
         const int u = e / R, j = e - u * R;
+        const int tu = u == 0 ? head.z : u == 1 ? head.w : u == 2 ? tail.x : tail.y;  // no local array
         float v = 0.f;
         if (u < nt)
-            for (int k = 0; k < s_parts; ++k) v += __ldcg(s_in + ((size_t)k * seg.n + tok[u]) * R + j);
+            for (int k = 0; k < s_parts; ++k) v += __ldcg(s_in + ((size_t)k * seg.n + tu) * R + j);
         ss[e] = v;
     }
-    const int o = blockIdx.y * 256 + threadIdx.x;
+    const int o = (blockIdx.y - blk0) * 256 + threadIdx.x;  // feature within the slice
     const bool live = o < h_out;
+    T* yc = y + sl.col + o;  // column of y
     float yv[kItemTok];
 #pragma unroll
-    for (int u = 0; u < kItemTok; ++u) yv[u] = live && u < nt ? to_f32(y[(size_t)tok[u] * h_out + o]) : 0.f;
+    for (int u = 0; u < kItemTok; ++u) yv[u] = live && u < nt ? to_f32(yc[(size_t)tok[u] * ldy]) : 0.f;
     __syncthreads();
     if (!live) return;
-    const T* Br = static_cast<const T*>(pool.B) + ((size_t)slot * h_out + o) * R;
+    const T* Br = static_cast<const T*>(sl.B) + ((size_t)slot * h_out + o) * R;
     float acc[kItemTok];
 #pragma unroll
     for (int u = 0; u < kItemTok; ++u) acc[u] = 0.f;
@@ -428,7 +452,7 @@ expand_seg_kernel(PoolView pool, SegView seg, const float* __restrict__ s_in, in
     }
 #pragma unroll
     for (int u = 0; u < kItemTok; ++u)
-        if (u < nt) y[(size_t)tok[u] * h_out + o] = from_f32<T>(yv[u] + acc[u]);
+        if (u < nt) yc[(size_t)tok[u] * ldy] = from_f32<T>(yv[u] + acc[u]);
 }
 
 // ---- CUDA-core base GEMM, optional fused expand ---------------------------------------------
@@ -507,14 +531,15 @@ int shrink_parts(const PoolView& pv, int n, bool tiled) {
 }
 
 template <typename T>
-static int launch_shrink_t(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st,
-                           bool tiled, int* s_parts) {
+static int launch_shrink_t(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,
+                           cudaStream_t st, bool tiled, int* s_parts) {
     const T* xp = static_cast<const T*>(x);
     *s_parts = shrink_parts(pv, sv.n, tiled);
     if constexpr (sizeof(T) == 2) {
         if (!tiled) {
             if (sv.n == 0) return LORA_OK;
-            void* args[] = {(void*)&pv, (void*)&sv, (void*)&xp, (void*)&s_out};
+            void* args[] = {(void*)&pv, (void*)&grp, (void*)&sv, (void*)&xp, (void*)&s_out};
+            const int rows = grp.count * (pv.R / 8);  // (slice, 8-row group) pairs
             // Per token, every LoRA token re-reads its adapter's A rows: n * r_max * h_in * 2
             // bytes at most.  Past 16 MB (r_max 64 at 64 tokens, 4096 features: 33.5 MB) the
             // segmented kernel reads each adapter once per 4 tokens instead (GB300, 32 chained
@@ -523,15 +548,16 @@ static int launch_shrink_t(const PoolView& pv, const SegView& sv, const void* x,
             if ((double)sv.n * pv.R * pv.h_in * 2 >= 16.0 * (1 << 20)) {
                 // at most one item per LoRA token, and per segment one partial item beyond n / 4
                 const int items = std::min(sv.n, std::min(sv.n, pv.S) + (sv.n + kItemTok - 1) / kItemTok);
-                LORA_CUDA_TRY(launch_pdl((const void*)shrink_seg_kernel<T>, dim3(items, pv.R / 8, *s_parts), dim3(128),
-                                         0, st, args));
+                LORA_CUDA_TRY(launch_pdl((const void*)shrink_seg_kernel<T>, dim3(items, rows, *s_parts), dim3(128), 0,
+                                         st, args));
             } else {
-                LORA_CUDA_TRY(launch_pdl((const void*)shrink_token_kernel<T>, dim3(sv.n, pv.R / 8, *s_parts), dim3(128),
-                                         0, st, args));
+                LORA_CUDA_TRY(launch_pdl((const void*)shrink_token_kernel<T>, dim3(sv.n, rows, *s_parts), dim3(128), 0,
+                                         st, args));
             }
             return LORA_OK;
         }
     }
+    if (grp.count != 1) return set_error(LORA_EUNSUP, "internal: grouped shrink needs 16-bit data and <= 256 tokens");
     if (!tiled) {
         const int RG = (pv.R % 8 == 0) ? 8 : 1;
         const long warps = (long)sv.n * (pv.R / RG);
@@ -558,28 +584,35 @@ static int launch_shrink_t(const PoolView& pv, const SegView& sv, const void* x,
 
 int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled,
                   int* s_parts) {
+    return launch_shrink_group(pv, single_group(pv), sv, x, s_out, st, tiled, s_parts);
+}
+
+int launch_shrink_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,
+                        cudaStream_t st, bool tiled, int* s_parts) {
     switch (pv.dtype) {
-        case LORA_F32: return launch_shrink_t<float>(pv, sv, x, s_out, st, tiled, s_parts);
-        case LORA_F16: return launch_shrink_t<__half>(pv, sv, x, s_out, st, tiled, s_parts);
-        default: return launch_shrink_t<__nv_bfloat16>(pv, sv, x, s_out, st, tiled, s_parts);
+        case LORA_F32: return launch_shrink_t<float>(pv, grp, sv, x, s_out, st, tiled, s_parts);
+        case LORA_F16: return launch_shrink_t<__half>(pv, grp, sv, x, s_out, st, tiled, s_parts);
+        default: return launch_shrink_t<__nv_bfloat16>(pv, grp, sv, x, s_out, st, tiled, s_parts);
     }
 }
 
 template <typename T>
-static int launch_expand_t(const PoolView& pv, const SegView& sv, const float* s_in, int s_parts, void* y,
-                           cudaStream_t st) {
+static int launch_expand_t(const PoolView& pv, const GroupView& grp, const SegView& sv, const float* s_in, int s_parts,
+                           void* y, cudaStream_t st) {
     if (sv.n == 0) return LORA_OK;
     T* yp = static_cast<T*>(y);
-    void* args[] = {(void*)&pv, (void*)&sv, (void*)&s_in, (void*)&s_parts, (void*)&yp};
     if constexpr (sizeof(T) == 2) {
-        // one CTA per (work item, 256 features); items: at most one per LoRA token, and per
-        // segment one partial item beyond n / 4
+        // one CTA per (work item, 256 features of a slice); items: at most one per LoRA token,
+        // and per segment one partial item beyond n / 4
+        void* args[] = {(void*)&pv, (void*)&grp, (void*)&sv, (void*)&s_in, (void*)&s_parts, (void*)&yp};
         const int items = std::min(sv.n, std::min(sv.n, pv.S) + (sv.n + kItemTok - 1) / kItemTok);
-        const dim3 grid(items, (pv.h_out + 255) / 256);
+        const dim3 grid(items, grp.blk[grp.count]);
         LORA_CUDA_TRY(launch_pdl((const void*)expand_seg_kernel<T>, grid, dim3(256), sizeof(float) * kItemTok * pv.R,
                                  st, args));
         return LORA_OK;
     }
+    if (grp.count != 1) return set_error(LORA_EUNSUP, "internal: grouped expand needs 16-bit data");
+    void* args[] = {(void*)&pv, (void*)&sv, (void*)&s_in, (void*)&s_parts, (void*)&yp};
     const dim3 grid((pv.h_out + 255) / 256, (sv.n + kExpTT - 1) / kExpTT);
     const size_t smem = sizeof(float) * kExpTT * pv.R;
     LORA_CUDA_TRY(launch_pdl((const void*)expand_kernel<T>, grid, dim3(256), smem, st, args));
@@ -587,10 +620,15 @@ static int launch_expand_t(const PoolView& pv, const SegView& sv, const float* s
 }
 
 int launch_expand(const PoolView& pv, const SegView& sv, const float* s_in, int s_parts, void* y, cudaStream_t st) {
+    return launch_expand_group(pv, single_group(pv), sv, s_in, s_parts, y, st);
+}
+
+int launch_expand_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const float* s_in, int s_parts,
+                        void* y, cudaStream_t st) {
     switch (pv.dtype) {
-        case LORA_F32: return launch_expand_t<float>(pv, sv, s_in, s_parts, y, st);
-        case LORA_F16: return launch_expand_t<__half>(pv, sv, s_in, s_parts, y, st);
-        default: return launch_expand_t<__nv_bfloat16>(pv, sv, s_in, s_parts, y, st);
+        case LORA_F32: return launch_expand_t<float>(pv, grp, sv, s_in, s_parts, y, st);
+        case LORA_F16: return launch_expand_t<__half>(pv, grp, sv, s_in, s_parts, y, st);
+        default: return launch_expand_t<__nv_bfloat16>(pv, grp, sv, s_in, s_parts, y, st);
     }
 }
 

@@ -59,14 +59,14 @@ inline int make_map_chunked(CUtensorMap* m, const void* base, int bf16, uint64_t
     return LORA_OK;
 }
 
-// Row-major [rows, cols] 16-bit matrix, box {box_cols, box_rows}, no swizzle (for stores of
-// row-major shared-memory tiles).
+// Row-major [rows, cols] 16-bit matrix with row stride ld elements (0: ld = cols), box
+// {box_cols, box_rows}, no swizzle (for stores of row-major shared-memory tiles).
 inline int make_map_plain(CUtensorMap* m, const void* base, int bf16, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                          uint32_t box_rows) {
+                          uint32_t box_rows, uint64_t ld = 0) {
     auto fn = encode_fn();
     if (!fn) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint64_t strides[1] = {(ld ? ld : cols) * 2};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,

@@ -227,3 +227,23 @@ def random_case(seed: int, n: int, h_in: int, h_out: int, ranks: Sequence[int],
     x = draw_x(rng, n, h_in, dtype)
     return LinearCase(f"random_s{seed}_n{n}_{h_in}x{h_out}", x, W, ad,
                       torch.from_numpy(np.asarray(idx, dtype=np.int32)))
+
+
+def random_group(seed: int, n: int, h_in: int, h_outs: Sequence[int], ranks: Sequence[int],
+                 r_max: Optional[int] = None, dtype: torch.dtype = torch.float16, p_base: float = 0.1,
+                 slice_ranks: Optional[Sequence[Sequence[int]]] = None) -> List[LinearCase]:
+    """Projections that share x and idx (q, k, v of one attention block): one case per slice,
+    all holding the same x and idx tensors, each with its own W and adapters (slot s of every
+    slice is mounted; ``slice_ranks[q]`` overrides the ranks of slice q).  Draw order: idx, x,
+    then W, A, B of every slice in turn."""
+    rng = _rng(seed, n, h_in, *h_outs)
+    S = len(ranks)
+    idx = torch.from_numpy(np.asarray(draw_zipf_idx(rng, n, S, p_base=p_base), dtype=np.int32))
+    x = draw_x(rng, n, h_in, dtype)
+    cases = []
+    for q, h_out in enumerate(h_outs):
+        rq = list(ranks if slice_ranks is None else slice_ranks[q])
+        W = draw_weight(rng, h_out, h_in, dtype)
+        ad = draw_adapters(rng, h_in, h_out, rq, [2.0 * r for r in rq], dtype, r_max=r_max)
+        cases.append(LinearCase(f"group_s{seed}_n{n}_{h_in}_slice{q}", x, W, ad, idx))
+    return cases

@@ -220,6 +220,39 @@ int lora_linear_fwd_static_ws(lora_pool_t pool, const void* W_dev, const void* x
  * measurements; host-only, no device access. */
 int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant);
 
+/* ---- grouped projections ---------------------------------------------------------------
+ *
+ * One adapter usually targets several projections of a layer (the registry entry of the
+ * ai.codenodex.com page, section "适配器先进入可信注册表", lists target modules q_proj and
+ * v_proj), and the projections of an attention block (q, k, v) or of an MLP (gate, up)
+ * read the same x and route every token to the same adapter.  A group runs such
+ * projections as one linear over their row-concatenated base weight, sharing one
+ * segment table, one pass over x for the shrink and one launch per kernel:
+ *
+ *     y[:, col_q : col_q + h_out_q] = x W_q^T + (alpha_s / r_s) (x A_{q,s}^T) B_{q,s}^T
+ *
+ * for slice q = 0..count-1, with col_q = h_out_0 + ... + h_out_{q-1}.
+ *   count   1..4 slices; pools[q] is slice q's adapter pool.  Every pool has the same h_in,
+ *           r_max, n_slots and dtype (fp16 or bf16; otherwise LORA_EUNSUP), and the same
+ *           slots mounted (LORA_EINVAL otherwise; checked against the host-side record of
+ *           mounts, so each slot's adapter is mounted into every pool of the group).
+ *           With count > 1 every h_out_q is a multiple of 16.
+ *   W_dev   [sum h_out_q, h_in]: the slices' base weights stacked row-wise (slice 0 first).
+ *   x_dev   [n, h_in];  y_dev [n, sum h_out_q]: slice q's output is its column range.
+ *           W, x, y 16-byte aligned, n = seg->n_tokens, seg from lora_segment on pools[0].
+ *   ws_dev  >= lora_linear_group_workspace_bytes, 256-byte aligned.
+ *   variant LORA_VARIANT_AUTO (lora_linear_group_policy), FUSED or SEPARATE; the CUDA-core
+ *           diagnostic variant is LORA_EUNSUP.
+ * Errors and the device status word behave as in lora_linear_fwd (y untouched when the
+ * segments carry an error).  A group of one is the same computation as lora_linear_fwd. */
+int lora_linear_group_workspace_bytes(int count, const lora_pool_t* pools, int n_tokens, size_t* bytes);
+int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev, const void* x_dev, void* y_dev,
+                          const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes, void* stream);
+/* Which variant AUTO picks for a group (1 or 2): separate -- one base GEMM over the
+ * concatenated weight, then one segmented expand over every slice -- for batches of up to
+ * 256 tokens, fused above.  Measured on GB300; host-only. */
+int lora_linear_group_policy(int count, const lora_pool_t* pools, int n_tokens, int* variant);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* lora_last_error(void);
 

@@ -33,6 +33,8 @@ What it computes, in float64, straight from the definitions:
   base model or to another adapter (ai.codenodex.com page, section
   "请求身份决定适配器，而非客户端参数": default deny, a missing mapping is an error).
 
+* ``lora_linear_group``: projections sharing x and idx, side by side (see its docstring).
+
 Pins (tests/test_oracle_pins.py): brute force in pure-Python loops on tiny inputs,
 numpy's stable argsort for the segment order, the merged-weight identity, zero-pad
 invariance, permutation equivariance, the unit-vector selector closed form, the
@@ -178,6 +180,19 @@ def lora_linear(x, W, pool: OraclePool, idx, rows: Optional[Sequence[int]] = Non
         u = pool.A[s] @ xs[i]  # shrink: [r_max]
         y[i] += pool.scale[s] * (pool.B[s] @ u)  # expand: [h_out]
     return y
+
+
+def lora_linear_group(x, Ws: Sequence, pools: Sequence[OraclePool], idx,
+                      rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Several projections that read the same x with the same token-to-adapter map (q, k
+    and v of one attention block): slice q is ``lora_linear`` of W_q with pool q, and the
+    result puts the slices side by side, slice 0's columns first.
+
+    One adapter identity covers all of its target modules (the registry entry of the
+    ai.codenodex.com page, section "适配器先进入可信注册表", lists target modules q_proj
+    and v_proj), so an idx must be valid in every pool of the group.
+    """
+    return np.concatenate([lora_linear(x, W, p, idx, rows=rows) for W, p in zip(Ws, pools)], axis=1)
 
 
 def lora_linear_case(case, rows=None) -> np.ndarray:

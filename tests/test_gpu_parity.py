@@ -362,3 +362,157 @@ def test_full_layer_sampled(lib):
     for case in cases:
         y, pool, seg = run(lib, case, 0)
         assert_parity(y[rows], O.lora_linear_case(case, rows=rows), case.name)
+
+
+# ------------------------------------------------------------------------------------------
+# segments shared by pools whose slots hold different ranks
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_segments_shared_with_a_pool_of_larger_ranks(lib, variant):
+    """The shrink work items carry the ranks of the pool the segments were built on; a pool
+    that holds the same slots at larger ranks (r_max 64, 64 tokens: the segmented shrink)
+    must still apply every row of its own adapters."""
+    small = wl.random_case(50, 64, 4096, 256, [8, 8, 16], r_max=64, dtype=torch.float16)
+    big = wl.random_case(51, 64, 4096, 256, [64, 40, 64], r_max=64, dtype=torch.float16,
+                         idx=small.idx.numpy())
+    pool_small, pool_big = make_pool(lib, small), make_pool(lib, big)
+    seg = pool_small.segment(small.idx.to(DEV))
+    y = pool_big.linear(big.W.to(DEV), big.x.to(DEV), seg, variant=variant).cpu()
+    assert_parity(y, O.lora_linear_case(big), f"shared segments variant {variant}")
+    y0 = pool_big.linear(torch.zeros_like(big.W).to(DEV), big.x.to(DEV), seg, variant=variant).cpu()
+    assert_lora_only_parity(y0, O.lora_linear(big.x, torch.zeros_like(big.W), O.pool_of_case(big),
+                                              big.idx.numpy()), f"shared segments W=0 variant {variant}")
+
+
+# ------------------------------------------------------------------------------------------
+# grouped projections: slices sharing x and segments, one concatenated weight
+# ------------------------------------------------------------------------------------------
+
+def group_pools(ags, cases):
+    return [make_pool(ags, c) for c in cases]
+
+
+def run_group(ags, cases, variant=0, pools=None, zero_w=False, ws=None):
+    pools = pools or group_pools(ags, cases)
+    x, idx = cases[0].x.to(DEV), cases[0].idx.to(DEV)
+    seg = pools[0].segment(idx)
+    W = torch.cat([c.W for c in cases], 0).to(DEV)
+    if zero_w:
+        W.zero_()
+    n = cases[0].n
+    y = torch.full((n, W.shape[0]), float("nan"), dtype=cases[0].dtype, device=DEV)
+    handles = [p.handle for p in pools]
+    if ws is None:
+        ws = ags._device_bytes(ags.lora_linear_group_workspace_bytes(handles, n), DEV)
+    ags.lora_linear_fwd_group(handles, W, x, y, seg, ws, variant)
+    torch.cuda.synchronize()
+    return y.cpu(), pools, seg
+
+
+def group_ref(cases, zero_w=False):
+    Ws = [torch.zeros_like(c.W) if zero_w else c.W for c in cases]
+    return O.lora_linear_group(cases[0].x, Ws, [O.pool_of_case(c) for c in cases], cases[0].idx.numpy())
+
+
+GROUPS = [
+    # (seed, n, h_in, slice h_out, ranks, r_max, dtype)
+    (40, 16, 256, [256, 128, 128], [8, 8, 8], 8, torch.float16),  # q, k, v with narrower k/v
+    (41, 64, 1024, [512, 512, 512], [8, 16, 8, 16], 16, torch.bfloat16),
+    (42, 1, 512, [256, 256], [8], 8, torch.float16),
+    (43, 100, 4104, [384, 128], [16, 8, 16, 16, 4], 16, torch.bfloat16),  # ragged K
+    (44, 256, 512, [176, 304], [16, 8, 16], 16, torch.bfloat16),  # slice edges inside tiles
+    (45, 64, 4096, [512, 256], [64, 8, 64], 64, torch.float16),  # segmented shrink, 2 slices
+    (46, 300, 512, [256, 128, 128], [16, 16], 16, torch.bfloat16),  # prefill path
+    (47, 700, 256, [272, 528], [8, 8, 8], 8, torch.float16),  # prefill, slice edge inside a tile
+    (48, 130, 256, [128, 128, 128, 128], [8, 8], 8, torch.float16),  # four slices
+]
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("spec", GROUPS, ids=[f"n{s[1]}_{s[2]}x{'+'.join(map(str, s[3]))}" for s in GROUPS])
+def test_group_parity(lib, spec, variant):
+    seed, n, h_in, h_outs, ranks, r_max, dtype = spec
+    cases = wl.random_group(seed, n, h_in, h_outs, ranks, r_max=r_max, dtype=dtype, p_base=0.15)
+    y, pools, _ = run_group(lib, cases, variant)
+    assert_parity(y, group_ref(cases), f"group {seed} variant {variant}")
+    y0, _, _ = run_group(lib, cases, variant, pools=pools, zero_w=True)
+    assert_lora_only_parity(y0, group_ref(cases, zero_w=True), f"group {seed} W=0 variant {variant}")
+    # negative control: every LoRA token moved to another adapter must not pass
+    idx = cases[0].idx.numpy()
+    if (idx >= 0).any():
+        S = len(ranks)
+        moved = np.where(idx >= 0, (idx + 1) % S if S > 1 else -1, idx).astype(np.int32)
+        wrong = O.lora_linear_group(cases[0].x, [torch.zeros_like(c.W) for c in cases],
+                                    [O.pool_of_case(c) for c in cases], moved)
+        assert not O.within_tolerance(y0, wrong).all()
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("n", [16, 64, 300])
+def test_group_of_one_is_the_single_linear(lib, n, variant):
+    case = wl.random_case(60, n, 512, 384, [8, 16, 8], r_max=16, dtype=torch.bfloat16)
+    y1, pools, seg = run_group(lib, [case], variant)
+    y = pools[0].linear(case.W.to(DEV), case.x.to(DEV), seg, variant=variant).cpu()
+    assert torch.equal(y1, y)
+
+
+def test_group_slices_with_different_ranks(lib):
+    cases = wl.random_group(61, 64, 4096, [256, 256], [8, 8, 8], r_max=64, dtype=torch.float16,
+                            slice_ranks=[[8, 8, 8], [64, 33, 64]])
+    for variant in (1, 2):
+        y0, _, _ = run_group(lib, cases, variant, zero_w=True)
+        assert_lora_only_parity(y0, group_ref(cases, zero_w=True), f"mixed slice ranks variant {variant}")
+
+
+def test_group_errors(lib):
+    cases = wl.random_group(62, 16, 256, [128, 128], [8, 8], dtype=torch.float16)
+    pools = group_pools(lib, cases)
+    handles = [p.handle for p in pools]
+    x, W = cases[0].x.to(DEV), torch.cat([c.W for c in cases], 0).to(DEV)
+    y = torch.zeros(16, 256, dtype=torch.float16, device=DEV)
+    seg = pools[0].segment(cases[0].idx.to(DEV))
+    ws = lib._device_bytes(lib.lora_linear_group_workspace_bytes(handles, 16), DEV)
+
+    def code(fn):
+        with pytest.raises(lib.LoraError) as e:
+            fn()
+        return e.value.code
+
+    assert code(lambda: lib.lora_linear_fwd_group([], W, x, y, seg, ws)) == lib.LORA_EINVAL
+    assert code(lambda: lib.lora_linear_fwd_group(handles * 3, W, x, y, seg, ws)) == lib.LORA_EINVAL  # 6 > 4
+    assert code(lambda: lib.lora_linear_fwd_group(handles, W, x, y, seg, ws, 3)) == lib.LORA_EUNSUP
+    small_ws = lib._device_bytes(256, DEV)
+    assert code(lambda: lib.lora_linear_fwd_group(handles, W, x, y, seg, small_ws)) == lib.LORA_ENOSPACE
+    other = lib.LoraPool(512, 128, 8, 2, torch.float16, DEV)  # different h_in
+    assert code(lambda: lib.lora_linear_fwd_group([handles[0], other.handle], W, x, y, seg, ws)) == lib.LORA_EINVAL
+    ragged = lib.LoraPool(256, 136, 8, 2, torch.float16, DEV)  # h_out not a multiple of 16
+    for s in range(2):
+        ragged.load_slot(s, cases[0].adapters.A[s].to(DEV), torch.zeros(136, 8, dtype=torch.float16, device=DEV), 16.0)
+    assert code(lambda: lib.lora_linear_group_workspace_bytes([handles[0], ragged.handle], 16)) == lib.LORA_EINVAL
+    partial = lib.LoraPool(256, 128, 8, 2, torch.float16, DEV)  # slot 1 not mounted
+    partial.load_slot(0, cases[1].adapters.A[0].to(DEV), cases[1].adapters.B[0].to(DEV), 16.0)
+    assert code(lambda: lib.lora_linear_fwd_group([handles[0], partial.handle], W, x, y, seg, ws)) == lib.LORA_EINVAL
+    f32 = lib.LoraPool(256, 128, 8, 2, torch.float32, DEV)
+    assert code(lambda: lib.lora_linear_group_workspace_bytes([f32.handle], 16)) == lib.LORA_EUNSUP
+    assert torch.count_nonzero(y) == 0  # nothing ran
+    assert lib.lora_linear_group_policy(handles, 64) == lib.LORA_VARIANT_SEPARATE
+    assert lib.lora_linear_group_policy(handles, 4096) == lib.LORA_VARIANT_FUSED
+
+
+@pytest.mark.parametrize("n", [16, 300])
+def test_group_invalid_idx_leaves_y_untouched(lib, n):
+    cases = wl.random_group(63, n, 256, [128, 256], [8, 8], dtype=torch.bfloat16)
+    pools = group_pools(lib, cases)
+    idx = cases[0].idx.clone()
+    idx[n // 2] = 7  # no such slot
+    seg = pools[0].segment(idx.to(DEV))
+    handles = [p.handle for p in pools]
+    W = torch.cat([c.W for c in cases], 0).to(DEV)
+    y = torch.full((n, 384), 3.0, dtype=torch.bfloat16, device=DEV)
+    ws = lib._device_bytes(lib.lora_linear_group_workspace_bytes(handles, n), DEV)
+    for variant in (1, 2):
+        lib.lora_linear_fwd_group(handles, W, cases[0].x.to(DEV), y, seg, ws, variant)
+        torch.cuda.synchronize()
+        assert lib.lora_segment_status(seg) == lib.LORA_EIDX
+        assert torch.all(y == 3.0)

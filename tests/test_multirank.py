@@ -54,20 +54,23 @@ def test_single_process_helpers():
     assert bench.rank_seed_offset(0) == 0 and bench.rank_seed_offset(1) != 0
 
 
-def test_profile_traffic_is_read_for_the_current_source(tmp_path, monkeypatch):
-    # the committed ncu summaries carry the GEMM source hash they were taken on; the bench
-    # reports their DRAM bytes only while the source is unchanged
-    traffic = bench.read_profile_traffic("gemm_decode_decode")
-    assert traffic is not None and traffic > 3.3e7  # at least the 4096 x 4096 fp16 weight
-    assert bench.read_profile_traffic("gemm_prefill_prefill") is not None
-    assert bench.read_profile_traffic("no_such_profile") is None
-    fake = tmp_path / "profiles"
-    fake.mkdir()
-    (fake / "gemm_decode_decode.md").write_text(
-        "- gemm_tc.cu sha256[:16]: 0000000000000000\n- dram bytes per launch (full workload): 123\n")
+def test_profile_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    # an ncu summary carries the hash of the GEMM source it was taken on; the bench reports
+    # its DRAM bytes only while that source is unchanged
+    import hashlib
+
     csrc = tmp_path / "adapter_gemm_segment_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    src = os.path.join(bench.ROOT, "adapter_gemm_segment_gb300", "csrc", "gemm_tc.cu")
-    (csrc / "gemm_tc.cu").write_bytes(open(src, "rb").read())
+    src = b"// a kernel source\n"
+    (csrc / "gemm_tc.cu").write_bytes(src)
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    (prof / "gemm_decode_decode.md").write_text(
+        f"# summary\n- gemm_tc.cu sha256[:16]: {sha}\n- dram bytes per launch (full workload): 35937024\n")
+    (prof / "gemm_prefill_prefill.md").write_text(
+        "- gemm_tc.cu sha256[:16]: 0000000000000000\n- dram bytes per launch (full workload): 123\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.read_profile_traffic("gemm_decode_decode") is None  # hash of another source
+    assert bench.read_profile_traffic("gemm_decode_decode") == 35937024.0
+    assert bench.read_profile_traffic("gemm_prefill_prefill") is None  # taken on another source
+    assert bench.read_profile_traffic("no_such_profile") is None

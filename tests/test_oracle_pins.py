@@ -211,8 +211,67 @@ def pin_errors(O):
     return True, ""
 
 
+def tiny_group(seed, n=6, h_in=5, h_outs=(3, 4, 2), ranks=((1, 2), (2, 2), (3, 1)), r_max=3):
+    """Slices sharing x and idx; ranks[q][s] is slice q's rank for slot s."""
+    rng = np.random.default_rng(seed)
+    S = len(ranks[0])
+    idx = np.where(rng.random(n) < 0.25, -1, rng.integers(0, S, n)).astype(np.int32)
+    x = rng.standard_normal((n, h_in))
+    Ws, slices = [], []
+    for h_out, rq in zip(h_outs, ranks):
+        Ws.append(rng.standard_normal((h_out, h_in)))
+        slices.append([(rng.standard_normal((r, h_in)), rng.standard_normal((h_out, r)), r,
+                        float(rng.integers(1, 33))) for r in rq])
+    return x, Ws, slices, idx, r_max
+
+
+def pin_group_block_diagonal(O):
+    """The group equals one linear over the stacked weight whose LoRA term, per token, is a
+    block-diagonal B (every slice's B_s on the diagonal) applied to the stacked, scaled A_s x."""
+    from scipy.linalg import block_diag
+
+    for seed in range(4):
+        x, Ws, slices, idx, r_max = tiny_group(20 + seed)
+        pools = [make_pool(O, ads, r_max, x.shape[1], W.shape[0]) for W, ads in zip(Ws, slices)]
+        y = O.lora_linear_group(x, Ws, pools, idx)
+        want = x @ np.vstack(Ws).T
+        for t, s in enumerate(idx.tolist()):
+            if s < 0:
+                continue
+            A_stack = np.vstack([(ads[s][3] / ads[s][2]) * ads[s][0] for ads in slices])
+            B_blk = block_diag(*[ads[s][1] for ads in slices])
+            want[t] += B_blk @ (A_stack @ x[t])
+        if y.shape != want.shape or not np.allclose(y, want, rtol=1e-12, atol=1e-12):
+            return False, f"seed {seed}: block-diagonal form differs"
+    return True, ""
+
+
+def pin_group_brute_force(O):
+    x, Ws, slices, idx, r_max = tiny_group(30, n=5)
+    pools = [make_pool(O, ads, r_max, x.shape[1], W.shape[0]) for W, ads in zip(Ws, slices)]
+    y = O.lora_linear_group(x, Ws, pools, idx)
+    cols = [brute_force(x.tolist(), W.tolist(), ads, idx.tolist(), r_max) for W, ads in zip(Ws, slices)]
+    want = np.array([sum((c[t] for c in cols), []) for t in range(len(idx))])
+    if y.shape != want.shape or not np.allclose(y, want, rtol=1e-12, atol=1e-12):
+        return False, "group differs from per-slice brute force side by side"
+    return True, ""
+
+
+def pin_group_errors(O):
+    x, Ws, slices, idx, r_max = tiny_group(31)
+    pools = [make_pool(O, ads, r_max, x.shape[1], W.shape[0]) for W, ads in zip(Ws, slices)]
+    # slice 1 holds slot 0 only (slot 1 of the same identity is missing there)
+    pools[1] = make_pool(O, slices[1][:1], r_max, x.shape[1], Ws[1].shape[0], n_slots=2)
+    try:
+        O.lora_linear_group(x, Ws, pools, np.array([0, 1, -1, 0, 0, 1], np.int32))
+    except O.OracleError as e:
+        return (e.code == O.EIDX), "wrong error code"
+    return False, "slot missing from one slice accepted"
+
+
 PINS = [pin_golden, pin_brute_force, pin_segments_argsort, pin_base_only, pin_merged_weight,
-        pin_zero_pad, pin_permutation, pin_selector, pin_rank1, pin_errors]
+        pin_zero_pad, pin_permutation, pin_selector, pin_rank1, pin_errors, pin_group_block_diagonal,
+        pin_group_brute_force, pin_group_errors]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -242,6 +301,10 @@ MUTANTS = {
     "base_only_sorted_last": ("count[k + 1] += 1", "count[(k + 1) if k >= 0 else S] += 1"),
     "scale_missing": ("y[i] += pool.scale[s] * (pool.B[s] @ u)", "y[i] += (pool.B[s] @ u)"),
     "no_validation": ("if k < -1 or k >= S:", "if False:"),
+    "group_slices_in_reverse": ("[lora_linear(x, W, p, idx, rows=rows) for W, p in zip(Ws, pools)]",
+                                "[lora_linear(x, W, p, idx, rows=rows) for W, p in zip(Ws, pools)][::-1]"),
+    "group_one_pool_for_all": ("[lora_linear(x, W, p, idx, rows=rows) for W, p in zip(Ws, pools)]",
+                               "[lora_linear(x, W, pools[0], idx, rows=rows) for W, p in zip(Ws, pools)]"),
 }
 
 
