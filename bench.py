@@ -52,6 +52,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["decode", "prefill", "mixed", "layer", "load"], default="decode")
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 fused, 2 separate, 3 CUDA-core")
+    p.add_argument("--ungrouped", action="store_true",
+                   help="layer and prefill workloads: one call per projection instead of grouping the projections "
+                        "that read the same x (q|k|v and gate|up; q|v)")
     p.add_argument("--layers", type=int, default=None, help="layer copies per step (32; 4 for --workload layer)")
     p.add_argument("--tokens", type=int, default=64, help="batch size of the decode/mixed workloads")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the cpu_baseline leg")
@@ -371,6 +374,7 @@ def ours(args):
 
     # ---- device-resident inputs, pools, workspaces ----
     layers = []
+    x_dev = {}  # projections fed by the same input (q, k, v; gate, up) share one device copy
     for case in cases:
         ad = case.adapters
         pool = ags.LoraPool(case.h_in, case.h_out, ad.r_max, ad.n_slots, dtype, dev)
@@ -378,7 +382,9 @@ def ours(args):
         B_all = [b.to(dev, non_blocking=True) for b in ad.B]
         for s in range(ad.n_slots):
             pool.load_slot(s, A_all[s], B_all[s], ad.alphas[s])
-        layers.append({"pool": pool, "W": case.W.to(dev), "x": case.x.to(dev),
+        if id(case.x) not in x_dev:
+            x_dev[id(case.x)] = case.x.to(dev)
+        layers.append({"pool": pool, "W": case.W.to(dev), "x": x_dev[id(case.x)],
                        "y": torch.empty(n, case.h_out, dtype=dtype, device=dev)})
         del A_all, B_all
     # prefill: q and v share x
@@ -393,16 +399,45 @@ def ours(args):
 
     launches_before = ags.lora_kernel_launch_count()
 
-    prefetch = args.prefetch_next and args.workload != "prefill"
-    nxt = [layers[(i + 1) % len(layers)]["W"] if prefetch else None for i in range(len(layers))]
+    # calls of one step: single linears, or (layer workload) groups of projections that read
+    # the same x -- q|k|v and gate|up -- as one call over their concatenated weight
+    calls = []
+    grouped = args.workload in ("layer", "prefill") and not args.ungrouped
+    i = 0
+    while i < len(layers):
+        j = i + 1
+        while grouped and j < len(layers) and layers[j]["x"] is layers[i]["x"] and j - i < 4:
+            j += 1
+        members = layers[i:j]
+        if len(members) == 1:
+            calls.append({"members": members, "y": members[0]["y"]})
+        else:
+            handles = [L["pool"].handle for L in members]
+            calls.append({"members": members, "handles": handles,
+                          "W": torch.cat([L["W"] for L in members], 0), "x": members[0]["x"],
+                          "y": torch.empty(n, sum(L["W"].shape[0] for L in members), dtype=dtype, device=dev)})
+            lin_ws = lin_ws if lin_ws.numel() >= ags.lora_linear_group_workspace_bytes(handles, n) else \
+                ags._device_bytes(ags.lora_linear_group_workspace_bytes(handles, n), dev)
+            for L in members:  # the group reads the concatenated weight and writes the concatenated output
+                L["W"] = L["y"] = None
+        i = j
+    torch.cuda.synchronize()
 
-    def linear(i, L, seg):
-        ags.lora_linear_fwd_ex(L["pool"].handle, L["W"], L["x"], L["y"], seg, lin_ws, args.variant, prefetch=nxt[i])
+    prefetch = args.prefetch_next and args.workload != "prefill" and not grouped
+    nxt = [calls[(i + 1) % len(calls)]["members"][0]["W"] if prefetch else None for i in range(len(calls))]
+
+    def linear(i, c, seg):
+        if "handles" in c:
+            ags.lora_linear_fwd_group(c["handles"], c["W"], c["x"], c["y"], seg, lin_ws, args.variant)
+        else:
+            L = c["members"][0]
+            ags.lora_linear_fwd_ex(L["pool"].handle, L["W"], L["x"], L["y"], seg, lin_ws, args.variant,
+                                   prefetch=nxt[i])
 
     def step():
         seg = ags.lora_segment(idx_dev, pool0.handle, seg_ws)
-        for i, L in enumerate(layers):
-            linear(i, L, seg)
+        for i, c in enumerate(calls):
+            linear(i, c, seg)
 
     # eager warm-up (also checks the status word once)
     step()
@@ -450,7 +485,7 @@ def ours(args):
     value = job_tokens_per_s(world, tokens_per_step, args.steps, ms)
 
     # ---- per-kernel timing (events recorded around each kernel, graph-replayed) ----
-    n_lin = len(layers)
+    n_lin = len(calls)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_lin)]
     for trio in evs:
         for e in trio:
@@ -459,9 +494,9 @@ def ours(args):
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
         seg = ags.lora_segment(idx_dev, pool0.handle, seg_ws)
-        for i, (L, trio) in enumerate(zip(layers, evs)):
+        for i, (c, trio) in enumerate(zip(calls, evs)):
             ags.lora_set_timing_events(*trio)
-            linear(i, L, seg)
+            linear(i, c, seg)
         ags.lora_set_timing_events()
     reps = max(3, min(50, args.steps // 20))
     g2.replay()
@@ -511,7 +546,7 @@ def ours(args):
         xs = {id(L["x"]): L["x"] for L in layers}
         x_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu()) for k, v in xs.items()}
         idx_host = torch.empty(idx.shape, dtype=torch.int32, pin_memory=True).copy_(idx)
-        y_host = [torch.empty(L["y"].shape, dtype=dtype, pin_memory=True) for L in layers]
+        y_host = [torch.empty(c["y"].shape, dtype=dtype, pin_memory=True) for c in calls]
         h2d = idx_host.numel() * 4 + sum(v.numel() * v.element_size() for v in x_host.values())
         d2h = sum(y.numel() * y.element_size() for y in y_host)
         e2e_steps = max(3, min(args.steps, 500))
@@ -521,8 +556,8 @@ def ours(args):
             for k, v in xs.items():
                 v.copy_(x_host[k], non_blocking=True)
             graph.replay()
-            for L, yh in zip(layers, y_host):
-                yh.copy_(L["y"], non_blocking=True)
+            for c, yh in zip(calls, y_host):
+                yh.copy_(c["y"], non_blocking=True)
 
         for _ in range(3):
             e2e_step()
@@ -555,6 +590,8 @@ def ours(args):
                     "distinct_slots_touched": alg["D"], "lora_tokens": alg["n_L"],
                     "l2": "inputs larger than L2 (no flush)", "timing": "CUDA graph replay, CUDA events",
                     "l2_prefetch_next_weight": prefetch,
+                    "calls_per_step": len(calls),
+                    "grouped": "projections reading the same x as one call each (lora_linear_fwd_group)" if grouped else None,
                     "parallelism": f"replicas x{world} (token batches sharded across GPUs, no collective)"})
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
