@@ -295,6 +295,9 @@ int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev
     if (decode) {
         rc = launch_shrink_group(p0, grp, sv, x_dev, s_buf, st, /*tiled=*/false, &s_parts);  // every slice, one launch
         if (rc) return rc;
+    } else if (shrink_tc_group_supported(p0, count)) {
+        rc = launch_shrink_tc_group(p0, grp, sv, x_dev, s_buf, st);  // every slice, one launch
+        if (rc) return rc;
     } else {
         for (int q = 0; q < count; ++q) {
             float* s_q = s_buf + (size_t)q * grp.s_stride;

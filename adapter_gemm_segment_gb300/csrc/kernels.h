@@ -52,6 +52,11 @@ int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const v
 // Grouped tcgen05 shrink for batches of more than 256 tokens (one CTA per 128-token tile).
 int shrink_tc_supported(const PoolView& pv);
 int launch_shrink_tc(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st);
+// The same for the slices of a group in one launch (count * r_max <= 256): slice q's output
+// starts at s_out + q * grp.s_stride.
+int shrink_tc_group_supported(const PoolView& pv, int count);
+int launch_shrink_tc_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,
+                           cudaStream_t st);
 
 int num_sms();
 

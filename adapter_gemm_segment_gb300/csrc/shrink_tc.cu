@@ -30,15 +30,19 @@ constexpr size_t kShrSmem = (size_t)kShrStages * kShrStageBytes + 1024 + 4096;
 
 struct ShrinkArgs {
     PoolView pool;
+    GroupView grp;  // slices sharing x and idx; slice q's output at s_out + q * grp.s_stride
     SegView seg;
     float* s_out;
     int n, kb_total, bf16;
 };
 
+// The N operand of a pass holds, for each of its slots and then each slice, that slice's
+// r_max rows of the slot's A: a token's G * r_max accumulator columns are contiguous.
 template <typename T>
 __global__ void __launch_bounds__(kShrThreads, 1)
-shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA,
-                 const ShrinkArgs a) {
+shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA0,
+                 const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2,
+                 const __grid_constant__ CUtensorMap tmA3, const ShrinkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kShrStages * kShrStageBytes);
@@ -94,7 +98,9 @@ shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     if (q < kShrBM && !is_first) dloc[q] = fidx[q] >= 0 ? dloc[fidx[q]] : -1;
     if (D == 0) return;  // base-only tile: nothing to shrink
 
-    const int spp = kShrMaxN / R;  // slots per pass
+    const int G = a.grp.count;
+    const int GR = G * R;            // accumulator columns per slot
+    const int spp = kShrMaxN / GR;   // slots per pass
     const int passes = (D + spp - 1) / spp;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kShrStages; ++s) {
@@ -110,7 +116,7 @@ shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmX);
-        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmA0);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 2 * kShrMaxN);
@@ -127,7 +133,7 @@ shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             int it = 0;
             for (int p = 0; p < passes && !flags[0]; ++p) {
                 const int d0 = p * spp, dn = min(spp, D - d0);
-                const int rows = dn * R, rows_pad = (rows + 15) / 16 * 16;
+                const int rows = dn * GR, rows_pad = (rows + 15) / 16 * 16;
                 const uint32_t bytes = kShrXBytes + rows_pad * kShrBK * 2;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % kShrStages;
@@ -136,10 +142,16 @@ shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                     uint8_t* st = smem + s * kShrStageBytes;
                     tma_load_2d(st, &tmX, &full[s], kb * kShrBK, m0);
                     for (int d = 0; d < dn; ++d)
-                        tma_load_2d(st + kShrXBytes + d * R * 128, &tmA, &full[s], kb * kShrBK, dlist[d0 + d] * R);
-                    if (rows_pad > rows)  // r_max = 8 and an odd slot count: duplicate the last slot's rows
-                        tma_load_2d(st + kShrXBytes + rows * 128, &tmA, &full[s], kb * kShrBK,
-                                    dlist[d0 + dn - 1] * R);
+                        for (int q = 0; q < G; ++q) {
+                            const CUtensorMap* mA = q == 0 ? &tmA0 : q == 1 ? &tmA1 : q == 2 ? &tmA2 : &tmA3;
+                            tma_load_2d(st + kShrXBytes + (d * G + q) * R * 128, mA, &full[s], kb * kShrBK,
+                                        dlist[d0 + d] * R);
+                        }
+                    if (rows_pad > rows) {  // r_max = 8 and an odd row-block count: repeat the last block
+                        const int q = G - 1;
+                        const CUtensorMap* mA = q == 0 ? &tmA0 : q == 1 ? &tmA1 : q == 2 ? &tmA2 : &tmA3;
+                        tma_load_2d(st + kShrXBytes + rows * 128, mA, &full[s], kb * kShrBK, dlist[d0 + dn - 1] * R);
+                    }
                 }
             }
             if (flags[0]) {
@@ -158,7 +170,7 @@ shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             bool ok = true;
             for (int p = 0; p < passes && ok; ++p) {
                 const int buf = p & 1;
-                const int rows_pad = (min(spp, D - p * spp) * R + 15) / 16 * 16;
+                const int rows_pad = (min(spp, D - p * spp) * GR + 15) / 16 * 16;
                 const uint32_t idesc = idesc_f16(kShrBM, rows_pad, a.bf16 != 0);
                 if (!mbar_wait(&acc_empty[buf], ((p >> 1) & 1) ^ 1, flags)) {
                     ok = false;
@@ -190,28 +202,37 @@ shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         const int t = m0 + row;
         const int slot = tok_slot[row];
         const int dl = dloc[row];
-        const float scale = slot >= 0 ? a.pool.table[slot].scale : 0.f;
-        float* srow = a.s_out + (size_t)t * R;
+        float scale[kMaxGroup];  // alpha / r of the token's slot in every slice
+#pragma unroll
+        for (int q = 0; q < kMaxGroup; ++q)
+            scale[q] = (slot >= 0 && q < G) ? group_slice(a.grp, q).table[slot].scale : 0.f;
         for (int p = 0; p < passes; ++p) {
             const int buf = p & 1;
             const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (p >> 1) & 1, flags));
             if (!got) break;
             tc_fence_after();
             const int d0 = p * spp, dn = min(spp, D - d0);
-            const int rows_pad = (dn * R + 15) / 16 * 16;
+            const int rows_pad = (dn * GR + 15) / 16 * 16;
             const bool mine = slot >= 0 && dl >= d0 && dl < d0 + dn;
-            const int col0 = (dl - d0) * R;
+            const int col0 = (dl - d0) * GR;  // the token's G * r_max columns
             const uint32_t taddr = tmem + buf * kShrMaxN + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             for (int c0 = 0; c0 < rows_pad; c0 += 16) {
                 uint32_t r[16];
                 __syncwarp();
                 tmem_ld16(taddr + c0, r);
                 tmem_ld_wait();
-                if (mine && c0 + 16 > col0 && c0 < col0 + R) {
+                if (mine && c0 + 16 > col0 && c0 < col0 + GR) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const int col = c0 + c;
-                        if (col >= col0 && col < col0 + R) srow[col - col0] = scale * __uint_as_float(r[c]);
+                        const int col = c0 + c - col0;
+                        if (col >= 0 && col < GR) {
+                            const int q = col / R, j = col - q * R;
+                            float sc = scale[0];
+#pragma unroll
+                            for (int i = 1; i < kMaxGroup; ++i)
+                                if (i == q) sc = scale[i];
+                            a.s_out[q * a.grp.s_stride + (long long)t * R + j] = sc * __uint_as_float(r[c]);
+                        }
                     }
                 }
             }
@@ -225,17 +246,23 @@ shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
 }
 
 template <typename T>
-static int launch_shrink_tc_t(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st) {
+static int launch_shrink_tc_t(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,
+                              cudaStream_t st) {
     const int n = sv.n;
     if (n == 0) return LORA_OK;
+    if (grp.count < 1 || grp.count > kMaxGroup || grp.count * pv.R > kShrMaxN)
+        return set_error(LORA_EINVAL, "internal: tensor-core shrink of %d slices of rank %d", grp.count, pv.R);
     const int bf16 = pv.dtype == LORA_BF16;
-    CUtensorMap mX, mA;
+    CUtensorMap mX, mA[kMaxGroup];
     int rc = make_map(&mX, x, bf16, pv.h_in, n, kShrBM);
     if (rc) return rc;
-    rc = make_map(&mA, pv.A, bf16, pv.h_in, (uint64_t)pv.S * pv.R, pv.R);
-    if (rc) return rc;
+    for (int q = 0; q < kMaxGroup; ++q) {  // unused maps repeat slice 0's
+        rc = make_map(&mA[q], grp.A[q < grp.count ? q : 0], bf16, pv.h_in, (uint64_t)pv.S * pv.R, pv.R);
+        if (rc) return rc;
+    }
     ShrinkArgs a;
     a.pool = pv;
+    a.grp = grp;
     a.seg = sv;
     a.s_out = s_out;
     a.n = n;
@@ -247,7 +274,7 @@ static int launch_shrink_tc_t(const PoolView& pv, const SegView& sv, const void*
                                            (int)kShrSmem));
         attr_set = true;
     }
-    void* args[] = {(void*)&mX, (void*)&mA, (void*)&a};
+    void* args[] = {(void*)&mX, (void*)&mA[0], (void*)&mA[1], (void*)&mA[2], (void*)&mA[3], (void*)&a};
     LORA_CUDA_TRY(launch_pdl((const void*)shrink_tc_kernel<T>, dim3((n + kShrBM - 1) / kShrBM), dim3(kShrThreads),
                              kShrSmem, st, args));
     return LORA_OK;
@@ -261,8 +288,17 @@ int shrink_tc_supported(const PoolView& pv) {
 }
 
 int launch_shrink_tc(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st) {
-    if (pv.dtype == LORA_F16) return tc::launch_shrink_tc_t<__half>(pv, sv, x, s_out, st);
-    return tc::launch_shrink_tc_t<__nv_bfloat16>(pv, sv, x, s_out, st);
+    return launch_shrink_tc_group(pv, single_group(pv), sv, x, s_out, st);
+}
+
+int launch_shrink_tc_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,
+                           cudaStream_t st) {
+    if (pv.dtype == LORA_F16) return tc::launch_shrink_tc_t<__half>(pv, grp, sv, x, s_out, st);
+    return tc::launch_shrink_tc_t<__nv_bfloat16>(pv, grp, sv, x, s_out, st);
+}
+
+int shrink_tc_group_supported(const PoolView& pv, int count) {
+    return shrink_tc_supported(pv) && count >= 1 && count <= kMaxGroup && count * pv.R <= tc::kShrMaxN;
 }
 
 }  // namespace lora

@@ -426,6 +426,13 @@ GROUPS = [
     (46, 300, 512, [256, 128, 128], [16, 16], 16, torch.bfloat16),  # prefill path
     (47, 700, 256, [272, 528], [8, 8, 8], 8, torch.float16),  # prefill, slice edge inside a tile
     (48, 130, 256, [128, 128, 128, 128], [8, 8], 8, torch.float16),  # four slices
+    # prefill tensor-core shrink over every slice: slices x r_max = 256 (one slot per pass),
+    # an odd number of 8-row blocks (r_max 8, three slices), many slots per tile (several
+    # passes), and slices x r_max above 256 (one shrink launch per slice)
+    (49, 300, 256, [128, 128, 128, 128], [64, 8, 64], 64, torch.bfloat16),
+    (50, 500, 256, [256, 128, 128], [8, 4, 8, 8, 1], 8, torch.float16),
+    (51, 300, 256, [128, 128, 128], [16] * 20, 16, torch.bfloat16),
+    (52, 300, 256, [128, 256, 128], [128, 96], 128, torch.float16),
 ]
 
 
