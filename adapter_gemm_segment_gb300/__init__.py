@@ -5,11 +5,9 @@ Argument marshalling only: every step of the path runs in the CUDA library
 CPU or PyTorch fallback: if the library is missing or fails to load, importing this
 package raises.
 
-Same names as the C ABI (``lora_pool_bytes``, ``lora_pool_create``,
-``lora_pool_load_slot``, ``lora_pool_unload_slot``, ``lora_segment``,
-``lora_segment_status``, ``lora_linear_workspace_bytes``, ``lora_linear_fwd``,
-``lora_linear_policy``, ``lora_last_error``), plus a small ``LoraPool`` convenience
-wrapper that owns the pool's device buffer.
+Same names as the C ABI (the ``EXPORTED`` tuple: pool, segment, linear, grouped-linear and
+host-tier cache entry points), plus small ``LoraPool`` and ``LoraCache`` convenience wrappers;
+``LoraPool`` owns the pool's device buffer.
 """
 from __future__ import annotations
 
@@ -35,6 +33,8 @@ EXPORTED = (
     "lora_linear_fwd", "lora_linear_policy", "lora_last_error", "lora_kernel_launch_count",
     "lora_set_timing_events", "lora_linear_fwd_static_ws", "lora_linear_fwd_ex", "lora_pool_load_slots",
     "lora_linear_group_workspace_bytes", "lora_linear_fwd_group", "lora_linear_group_policy",
+    "lora_cache_create", "lora_cache_destroy", "lora_cache_register", "lora_cache_unregister", "lora_cache_map",
+    "lora_cache_slot_of", "lora_cache_stats",
 )
 
 
@@ -81,6 +81,13 @@ def _load() -> ctypes.CDLL:
         "lora_linear_group_workspace_bytes": [i32, P(vp), i32, P(sz)],
         "lora_linear_fwd_group": [i32, P(vp), vp, vp, vp, P(lora_segments), i32, vp, sz, vp],
         "lora_linear_group_policy": [i32, P(vp), i32, P(i32)],
+        "lora_cache_create": [i32, P(vp), P(vp)],
+        "lora_cache_destroy": [vp],
+        "lora_cache_register": [vp, ctypes.c_int64, P(vp), P(vp), P(i32), P(ctypes.c_float)],
+        "lora_cache_unregister": [vp, ctypes.c_int64, vp],
+        "lora_cache_map": [vp, P(ctypes.c_int64), i32, P(ctypes.c_int32), P(i32), vp],
+        "lora_cache_slot_of": [vp, ctypes.c_int64, P(i32)],
+        "lora_cache_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -287,6 +294,96 @@ def lora_linear_fwd_group(pool_handles, W: torch.Tensor, x: torch.Tensor, y: tor
                                       ctypes.byref(seg), variant, _ptr(_dev(ws, "ws")),
                                       ws.numel() * ws.element_size(), _stream(stream)))
     return y
+
+
+def lora_cache_create(pool_handles) -> ctypes.c_void_p:
+    count, arr = _handles(pool_handles)
+    h = ctypes.c_void_p()
+    _check(_lib.lora_cache_create(count, arr, ctypes.byref(h)))
+    return h
+
+
+def lora_cache_destroy(handle) -> None:
+    _check(_lib.lora_cache_destroy(handle))
+
+
+def lora_cache_register(handle, adapter_id: int, As, Bs, alphas) -> None:
+    """As[p], Bs[p]: pinned host tensors of pool p ([rank, h_in], [h_out, rank]); kept alive by
+    the caller until the adapter is unregistered."""
+    for t in list(As) + list(Bs):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("adapter tensors of the host tier must be contiguous pinned host memory")
+    n = len(As)
+    Ap = (ctypes.c_void_p * n)(*[a.data_ptr() for a in As])
+    Bp = (ctypes.c_void_p * n)(*[b.data_ptr() for b in Bs])
+    ranks = (ctypes.c_int * n)(*[int(a.shape[0]) for a in As])
+    al = (ctypes.c_float * n)(*[float(x) for x in alphas])
+    _check(_lib.lora_cache_register(handle, int(adapter_id), Ap, Bp, ranks, al))
+
+
+def lora_cache_unregister(handle, adapter_id: int, stream=None) -> None:
+    _check(_lib.lora_cache_unregister(handle, int(adapter_id), _stream(stream)))
+
+
+def lora_cache_map(handle, ids, stream=None):
+    """ids: adapter id per token (-1 = base only).  Returns (idx int32 CPU tensor, mounts)."""
+    ids = torch.as_tensor(ids, dtype=torch.int64).contiguous()
+    n = int(ids.numel())
+    idx = torch.empty(n, dtype=torch.int32)
+    mounts = ctypes.c_int()
+    _check(_lib.lora_cache_map(handle, ctypes.cast(ids.data_ptr(), ctypes.POINTER(ctypes.c_int64)), n,
+                               ctypes.cast(idx.data_ptr(), ctypes.POINTER(ctypes.c_int32)), ctypes.byref(mounts),
+                               _stream(stream)))
+    return idx, mounts.value
+
+
+def lora_cache_slot_of(handle, adapter_id: int) -> int:
+    out = ctypes.c_int()
+    _check(_lib.lora_cache_slot_of(handle, int(adapter_id), ctypes.byref(out)))
+    return out.value
+
+
+def lora_cache_stats(handle) -> dict:
+    h, m, e = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64()
+    _check(_lib.lora_cache_stats(handle, ctypes.byref(h), ctypes.byref(m), ctypes.byref(e)))
+    return {"hits": h.value, "misses": m.value, "evictions": e.value}
+
+
+class LoraCache:
+    """Host-tier adapter cache over pools (``LoraPool`` objects) with the same slot count."""
+
+    def __init__(self, pools):
+        self.pools = list(pools)
+        self.handle = lora_cache_create([p.handle for p in self.pools])
+        self._host = {}
+
+    def register(self, adapter_id: int, As, Bs, alphas) -> None:
+        lora_cache_register(self.handle, adapter_id, As, Bs, alphas)
+        self._host[int(adapter_id)] = (list(As), list(Bs))  # the host tier must stay alive
+
+    def unregister(self, adapter_id: int, stream=None) -> None:
+        lora_cache_unregister(self.handle, adapter_id, stream)
+        self._host.pop(int(adapter_id), None)
+
+    def map(self, ids, stream=None):
+        return lora_cache_map(self.handle, ids, stream)
+
+    def slot_of(self, adapter_id: int) -> int:
+        return lora_cache_slot_of(self.handle, adapter_id)
+
+    def stats(self) -> dict:
+        return lora_cache_stats(self.handle)
+
+    def close(self) -> None:
+        if self.handle is not None:
+            lora_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def segment_arrays(seg: lora_segments) -> dict:

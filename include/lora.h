@@ -253,6 +253,44 @@ int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev
  * 256 tokens, fused above.  Measured on GB300; host-only. */
 int lora_linear_group_policy(int count, const lora_pool_t* pools, int n_tokens, int* variant);
 
+/* ---- host-tier adapter cache -------------------------------------------------------------
+ *
+ * The blog.lonae.com page describes a tiered adapter store: hot adapters resident in GPU
+ * memory, warm ones in host memory, loaded on demand, unreferenced ones evicted.  A cache
+ * manages the slots of `count` pools with the same n_slots (typically every LoRA-augmented
+ * projection of a model) and keeps slot s of every pool holding the same adapter, so one
+ * segment table serves all of them.
+ *   lora_cache_create: the pools must hold no adapters (LORA_EBUSY otherwise); from then on
+ *     the cache owns their slots -- mounting or unmounting them directly breaks it.  The
+ *     pools must outlive the cache.
+ *   lora_cache_register: adapter `id` (>= 0) with, for pool p, A_host[p] [ranks[p], h_in_p]
+ *     and B_host[p] [h_out_p, ranks[p]] in the pool's dtype, in page-locked host memory (read
+ *     by the mount kernel over NVLink-C2C / PCIe; pageable memory is not accessible to it)
+ *     that the caller keeps valid until the adapter is unregistered.  LORA_EBUSY for a known
+ *     id, LORA_ERANK for a rank outside [1, r_max].  Nothing is copied yet.
+ *   lora_cache_map: for a batch of n tokens naming adapter ids (-1 = base only), makes every
+ *     named adapter resident and writes idx_out[t] (host int32: its slot, or -1), the input
+ *     of lora_segment.  A resident adapter is a hit; a missing one goes to a free slot, else
+ *     to the least recently used slot that this batch does not name (ties: lowest slot),
+ *     whose adapter is unmounted.  Mounts (one batched mount per pool) and unmounts are
+ *     enqueued on `stream`, so kernels enqueued later on that stream see them, and kernels
+ *     enqueued earlier still read the evicted adapter; work on other streams must be ordered
+ *     by the caller.  *mounts_out (may be NULL) = adapters mounted by this call.
+ *     An unregistered id is LORA_EIDX and more distinct ids than slots is LORA_ENOSPACE;
+ *     either way nothing changes and idx_out is not written.
+ *   lora_cache_unregister: forgets the adapter, unmounting it (on `stream`) if resident.
+ *   lora_cache_slot_of: the slot holding adapter id, or -1 if it is not resident.
+ *   lora_cache_stats: hits and misses (per distinct adapter per map call), evictions. */
+typedef struct lora_cache* lora_cache_t;
+int lora_cache_create(int count, const lora_pool_t* pools, lora_cache_t* out);
+int lora_cache_destroy(lora_cache_t cache);
+int lora_cache_register(lora_cache_t cache, int64_t id, const void* const* A_host, const void* const* B_host,
+                        const int* ranks, const float* alphas);
+int lora_cache_unregister(lora_cache_t cache, int64_t id, void* stream);
+int lora_cache_map(lora_cache_t cache, const int64_t* ids, int n, int32_t* idx_out, int* mounts_out, void* stream);
+int lora_cache_slot_of(lora_cache_t cache, int64_t id, int* slot);
+int lora_cache_stats(lora_cache_t cache, uint64_t* hits, uint64_t* misses, uint64_t* evictions);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* lora_last_error(void);
 

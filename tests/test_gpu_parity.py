@@ -523,3 +523,112 @@ def test_group_invalid_idx_leaves_y_untouched(lib, n):
         torch.cuda.synchronize()
         assert lib.lora_segment_status(seg) == lib.LORA_EIDX
         assert torch.all(y == 3.0)
+
+
+# ------------------------------------------------------------------------------------------
+# host-tier adapter cache: pinned host adapters, LRU eviction of slots the batch does not use
+# ------------------------------------------------------------------------------------------
+
+def lru_model(n_slots, batches):
+    """Independent model of the replacement rule: hits keep their slot; a miss takes the lowest
+    free slot, else the least recently used slot not named by the batch (ties: lowest slot)."""
+    slot_of, last, owner, clock, out = {}, [0] * n_slots, [None] * n_slots, 0, []
+    for ids in batches:
+        clock += 1
+        need = sorted({i for i in ids if i >= 0})
+        for i in need:
+            if i in slot_of:
+                last[slot_of[i]] = clock
+        for i in need:
+            if i in slot_of:
+                continue
+            free = [s for s in range(n_slots) if owner[s] is None]
+            if free:
+                s = free[0]
+            else:
+                cand = [s for s in range(n_slots) if last[s] != clock]
+                s = min(cand, key=lambda k: (last[k], k))
+                del slot_of[owner[s]]
+            owner[s], slot_of[i], last[s] = i, s, clock
+        out.append([slot_of[i] if i >= 0 else -1 for i in ids])
+    return out
+
+
+def test_cache_lru_mapping_and_parity(lib):
+    n_ad, S, n = 10, 4, 24
+    h_in, shapes, R = 256, [(256, 128), (256, 384)], 16  # two projections share the cache
+    rng = np.random.default_rng(70)
+    ranks = [int(r) for r in rng.choice([4, 8, 16], n_ad)]
+    host, oracle_ad = {}, {}
+    pools = [lib.LoraPool(hi, ho, R, S, torch.bfloat16, DEV) for hi, ho in shapes]
+    cache = lib.LoraCache(pools)
+    for a in range(n_ad):
+        As, Bs = [], []
+        for hi, ho in shapes:
+            As.append(torch.from_numpy(rng.uniform(-0.06, 0.06, (ranks[a], hi))).to(torch.bfloat16).pin_memory())
+            Bs.append(torch.from_numpy(rng.standard_normal((ho, ranks[a])) * 0.01).to(torch.bfloat16).pin_memory())
+        cache.register(100 + a, As, Bs, [2.0 * ranks[a]] * len(shapes))
+        oracle_ad[100 + a] = (As, Bs)
+    Ws = [torch.from_numpy(rng.standard_normal((ho, hi)) * 0.02).to(torch.bfloat16) for hi, ho in shapes]
+    batches = []
+    for b in range(6):  # each batch names at most S adapters
+        names = rng.choice(n_ad, size=int(rng.integers(1, S + 1)), replace=False) + 100
+        batches.append([int(rng.choice(names)) if rng.random() > 0.2 else -1 for _ in range(n)])
+    want_slots = lru_model(S, batches)
+    evictions = 0
+    for b, ids in enumerate(batches):
+        idx, mounts = cache.map(ids)
+        assert idx.tolist() == want_slots[b], f"batch {b}"
+        x = torch.from_numpy(rng.standard_normal((n, h_in))).to(torch.bfloat16)
+        seg = pools[0].segment(idx.to(DEV))
+        for q, (pool, W) in enumerate(zip(pools, Ws)):
+            y = pool.linear(W.to(DEV), x.to(DEV), seg, variant=0).cpu()
+            # the oracle sees the adapters by identity, not by slot
+            used = sorted({i for i in ids if i >= 0})
+            op = O.pad_pool([oracle_ad[i][0][q] for i in used], [oracle_ad[i][1][q] for i in used],
+                            [ranks[i - 100] for i in used], [2.0 * ranks[i - 100] for i in used], R, h_in,
+                            shapes[q][1])
+            local = np.array([used.index(i) if i >= 0 else -1 for i in ids], np.int32)
+            assert_parity(y, O.lora_linear(x, W, op, local), f"cache batch {b} projection {q}")
+            y0 = pool.linear(torch.zeros_like(W).to(DEV), x.to(DEV), seg, variant=0).cpu()
+            assert_lora_only_parity(y0, O.lora_linear(x, torch.zeros_like(W), op, local), f"cache W=0 {b}/{q}")
+    st = cache.stats()
+    assert st["hits"] + st["misses"] == sum(len({i for i in ids if i >= 0}) for ids in batches)
+    assert st["evictions"] > 0 and st["evictions"] == st["misses"] - min(S, st["misses"])
+    cache.close()
+
+
+def test_cache_errors(lib):
+    S = 2
+    pools = [lib.LoraPool(128, 128, 8, S, torch.float16, DEV)]
+    cache = lib.LoraCache(pools)
+    A = torch.zeros(8, 128, dtype=torch.float16).pin_memory()
+    B = torch.zeros(128, 8, dtype=torch.float16).pin_memory()
+    for i in range(3):
+        cache.register(i, [A], [B], [16.0])
+
+    def code(fn):
+        with pytest.raises(lib.LoraError) as e:
+            fn()
+        return e.value.code
+
+    assert code(lambda: cache.register(1, [A], [B], [16.0])) == lib.LORA_EBUSY
+    big = torch.zeros(16, 128, dtype=torch.float16).pin_memory()
+    assert code(lambda: cache.register(7, [big], [torch.zeros(128, 16, dtype=torch.float16).pin_memory()],
+                                       [1.0])) == lib.LORA_ERANK
+    assert code(lambda: cache.map([0, 5])) == lib.LORA_EIDX  # unknown adapter: nothing mounted
+    assert cache.slot_of(0) == -1 and cache.stats() == {"hits": 0, "misses": 0, "evictions": 0}
+    assert code(lambda: cache.map([0, 1, 2])) == lib.LORA_ENOSPACE  # three adapters, two slots
+    idx, mounts = cache.map([0, -1, 1, 0])
+    assert idx.tolist() == [0, -1, 1, 0] and mounts == 2
+    idx, mounts = cache.map([2, 1])  # 0 is least recently used and not named: evicted
+    assert idx.tolist() == [0, 1] and mounts == 1 and cache.slot_of(0) == -1
+    cache.unregister(2)
+    assert cache.slot_of(1) == 1 and code(lambda: cache.slot_of(2)) == lib.LORA_EIDX
+    busy = lib.LoraPool(128, 128, 8, S, torch.float16, DEV)
+    busy.load_slot(0, A.to(DEV), B.to(DEV), 16.0)
+    assert code(lambda: lib.LoraCache([busy])) == lib.LORA_EBUSY
+    other = lib.LoraPool(128, 128, 8, S + 1, torch.float16, DEV)
+    fresh = lib.LoraPool(128, 128, 8, S, torch.float16, DEV)
+    assert code(lambda: lib.LoraCache([fresh, other])) == lib.LORA_EINVAL  # slot counts differ
+    cache.close()
