@@ -20,6 +20,9 @@ struct lora_pool {
     void* A;
     void* B;
     std::vector<uint8_t> mounted;  // host mirror of the slot states this handle enqueued
+    std::vector<int> ranks;        // true rank of each mounted slot (host mirror)
+    bool top_dirty = true;         // top_chunks needs recomputing
+    int top_chunks[33] = {};       // see PoolView::top_chunks
 };
 
 namespace lora {
@@ -45,6 +48,10 @@ struct PoolView {
     const void* B;  // [S, h_out, R]
     int h_in, h_out, R, S;
     int dtype;      // lora_dtype
+    // top_chunks[k]: the largest number of 8-column chunks k slots can need at their true ranks
+    // (ceil(rank / 8); empty slots count as r_max / 8, the worst a later mount can bring).  Sizes
+    // the decode GEMM's staging of B tiles; the kernel re-checks the room it was given.
+    int top_chunks[33];
 };
 
 // Segments as the kernels see them (device pointers).

@@ -56,7 +56,8 @@ struct DecodeArgs {
     int nacc;     // independent TMEM accumulators the K-blocks rotate over (summed in the epilogue)
     int kc;       // 64-wide K chunks per pipeline stage (one TMA box per operand and stage)
     int s_parts;  // K-parts of the shrink output to sum
-    int dpre;     // distinct slots whose B rows are staged during the main loop
+    int bpre_bytes;  // room for B tiles staged during the main loop
+    int compact;     // stage each tile at its slot's true rank (else at r_max, no table read)
     int push;     // exchange partials by bulk copies (1) or remote loads (0)
     const char* prefetch;  // optional range streamed into L2 once this CTA's accumulator is complete
     size_t prefetch_bytes;
@@ -181,6 +182,56 @@ __device__ __forceinline__ void lora_batch8(const T* __restrict__ Bg, const floa
     }
 }
 
+// The same for slots staged at their true rank: staged slot d's tile is pre_sm[1 + kMaxPre + d]
+// chunk blocks of [128 rows][8 columns] (16 bytes per row), the first at uint4 offset
+// pre_sm[1 + d]; a warp's 32 consecutive rows read 32 consecutive 16-byte words.  Columns past
+// a slot's rank are zero in B and in s, so they are skipped; the loop runs over the largest
+// chunk count among the eight tokens.
+constexpr int kMaxPre = 32;
+
+template <typename T>
+__device__ __forceinline__ void lora_batch8_pre(const uint4* __restrict__ Bp4, const int* __restrict__ pre_sm,
+                                                const float* __restrict__ S_sm, const int* __restrict__ dloc_sm,
+                                                int q0, int cnt, int Dg, int row, int R, int lane, float (&acc)[8]) {
+    int off[8], c[8];
+    int cmax = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        int d = q0 + u < cnt ? dloc_sm[q0 + u] : -1;
+        if (d >= Dg) d = -1;
+        c[u] = d >= 0 ? pre_sm[1 + kMaxPre + d] : 0;
+        off[u] = d >= 0 ? pre_sm[1 + d] + row : 0;
+        cmax = max(cmax, c[u]);
+        acc[u] = 0.f;
+    }
+    for (int jc = 0; jc < cmax; ++jc) {
+        uint4 bv[8];
+        float4 s0[8], s1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            bv[u] = jc < c[u] ? Bp4[off[u] + jc * BM] : make_uint4(0, 0, 0, 0);
+            const float4* sp = reinterpret_cast<const float4*>(S_sm + min(q0 + u, cnt - 1) * R + jc * 8);
+            s0[u] = sp[0];
+            s1[u] = sp[1];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float b[8];
+            unpack8<T>(bv[u], b);
+            float v = acc[u];
+            v = fmaf(b[0], s0[u].x, v);
+            v = fmaf(b[1], s0[u].y, v);
+            v = fmaf(b[2], s0[u].z, v);
+            v = fmaf(b[3], s0[u].w, v);
+            v = fmaf(b[4], s1[u].x, v);
+            v = fmaf(b[5], s1[u].y, v);
+            v = fmaf(b[6], s1[u].z, v);
+            v = fmaf(b[7], s1[u].w, v);
+            acc[u] = v;
+        }
+    }
+}
+
 // ============================================================================================
 // decode: swap-AB + split-K over a thread-block cluster
 // ============================================================================================
@@ -199,7 +250,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmYtail,
-                   const DecodeArgs a) {
+                   const __grid_constant__ CUtensorMap tmB, const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
@@ -215,10 +266,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int* dloc_sm = slot_sm + per;                                               // [per]
     int* dlist = dloc_sm + per;                                                 // [per]
     int* fidx_sm = dlist + per;                                                 // [per]
-    float* S_sm = smem_align(reinterpret_cast<float*>(fidx_sm + per), 16);      // [s_parts][per][R]
+    int* pre_sm = fidx_sm + per;  // [1 + 2 kMaxPre]: staged slots; their uint4 offsets; chunks per row
+    float* S_sm = smem_align(reinterpret_cast<float*>(pre_sm + 1 + 2 * kMaxPre), 16);  // [s_parts][per][R]
     float* L_sm = S_sm + (size_t)a.s_parts * per * R;                            // [per][128] if use_lsm
-    T* Bpre = smem_align(reinterpret_cast<T*>(L_sm + (use_lsm ? (size_t)per * BM : 0)), 16);  // [dpre][128][R]
-    uint64_t* full = smem_align(reinterpret_cast<uint64_t*>(Bpre + (size_t)a.dpre * BM * R), 8);
+    T* Bpre = smem_align(reinterpret_cast<T*>(L_sm + (use_lsm ? (size_t)per * BM : 0)), 128);  // bpre_bytes
+    uint64_t* full = smem_align(reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(Bpre) + a.bpre_bytes), 8);
     uint64_t* empty = full + stages;
     uint64_t* tmem_full = empty + stages;
     uint64_t* lbar = tmem_full + 1;  // LoRA operands staged
@@ -275,6 +327,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         for (int i = 0; i < pre; ++i) issue_stage(i);
         prefetch_tmap(&tmY);
         prefetch_tmap(&tmYtail);
+        if (a.compact && a.fuse) prefetch_tmap(&tmB);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, a.tmem_cols);
@@ -384,22 +437,54 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 const int f = fidx_sm[q];
                 if (f != q) dloc_sm[q] = f >= 0 ? dloc_sm[f] : -1;
             }
-            const int Dg = min(running, a.dpre);
+            // compact staging: the slots' true ranks in whole 8-column chunks (this pool's table
+            // decides); otherwise every tile at r_max, without the dependent table read
+            if (a.compact) {
+                if (et < min(running, kMaxPre))
+                    pre_sm[1 + kMaxPre + et] = (min(max(__ldg(&a.pool.table[dlist[et]].rank), 1), R) + 7) / 8;
+                named_bar_sync(1, 128);
+            }
             if (et == 0) {
                 flags[2] = running;
-                // bulk copies: the owned tokens' shrink parts, then the pre-staged slots' B rows
                 const uint32_t s_bytes = static_cast<uint32_t>(cnt * R * 4);
-                const uint32_t b_bytes = static_cast<uint32_t>(rows_valid * R * 2);
-                const uint32_t total = (cnt > 0 ? a.s_parts * s_bytes : 0) + Dg * b_bytes;
-                mbar_arrive_expect_tx(lbar, total);
-                if (cnt > 0)
-                    for (int k = 0; k < a.s_parts; ++k)
-                        bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
-                for (int d = 0; d < Dg; ++d)
-                    bulk_g2s(Bpre + (size_t)d * BM * R, B + ((size_t)dlist[d] * h_out + m_tile * BM) * R, b_bytes,
-                             lbar);
+                if (a.compact) {
+                    // the first distinct slots whose true-rank tiles fit in the room planned
+                    int off = 0, ns = 0;
+                    for (int d = 0; d < min(running, kMaxPre); ++d) {
+                        const int c = pre_sm[1 + kMaxPre + d];
+                        if ((off + BM * c) * 16 > a.bpre_bytes) break;
+                        pre_sm[1 + d] = off;
+                        off += BM * c;
+                        ++ns;
+                    }
+                    pre_sm[0] = ns;
+                    // bulk copies of the owned tokens' shrink parts, then one TMA box per staged
+                    // slot and 8-column chunk: [128 feature rows][8 columns] of B
+                    mbar_arrive_expect_tx(lbar, (cnt > 0 ? a.s_parts * s_bytes : 0) + static_cast<uint32_t>(off) * 16);
+                    if (cnt > 0)
+                        for (int k = 0; k < a.s_parts; ++k)
+                            bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
+                    uint4* Bp4 = reinterpret_cast<uint4*>(Bpre);
+                    for (int d = 0; d < ns; ++d)
+                        for (int cc = 0; cc < pre_sm[1 + kMaxPre + d]; ++cc)
+                            tma_load_3d_cta(Bp4 + pre_sm[1 + d] + cc * BM, &tmB, lbar, 0, cc,
+                                            dlist[d] * h_out + m_tile * BM);
+                } else {
+                    // every tile at r_max ([128 rows][r_max], one contiguous bulk copy each)
+                    const uint32_t b_bytes = static_cast<uint32_t>(rows_valid * R * 2);
+                    const int ns = min(min(running, kMaxPre), a.bpre_bytes / (BM * R * 2));
+                    pre_sm[0] = ns;
+                    mbar_arrive_expect_tx(lbar, (cnt > 0 ? a.s_parts * s_bytes : 0) + ns * b_bytes);
+                    if (cnt > 0)
+                        for (int k = 0; k < a.s_parts; ++k)
+                            bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
+                    for (int d = 0; d < ns; ++d)
+                        bulk_g2s(Bpre + (size_t)d * BM * R, B + ((size_t)dlist[d] * h_out + m_tile * BM) * R, b_bytes,
+                                 lbar);
+                }
             }
             named_bar_sync(1, 128);
+            const int Dg = pre_sm[0];
             const bool staged = mbar_wait(lbar, 0, flags);
             // sum the shrink's K-parts once (part 0 receives the total)
             for (int e = et; e < cnt * R; e += 128) {
@@ -412,7 +497,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (use_lsm) {
                 for (int q0 = 0; q0 < cnt; q0 += 8) {
                     float acc[8];
-                    lora_batch8<T>(Bpre, S_sm, dloc_sm, q0, cnt, 0, staged ? Dg : 0, row, R, lane, acc);
+                    if (a.compact)
+                        lora_batch8_pre<T>(reinterpret_cast<const uint4*>(Bpre), pre_sm, S_sm, dloc_sm, q0, cnt,
+                                           staged ? Dg : 0, row, R, lane, acc);
+                    else
+                        lora_batch8<T>(Bpre, S_sm, dloc_sm, q0, cnt, 0, staged ? Dg : 0, row, R, lane, acc);
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         if (q0 + u < cnt) L_sm[(q0 + u) * BM + row] = acc[u];
@@ -497,16 +586,17 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     if (warp >= 2 && flags[1]) {
         float* own = P + (size_t)t0 * BM;  // this CTA's partials of its own tokens (LoRA added here)
         const int D = flags[2];
-        const int g_begin = use_lsm ? a.dpre : 0;  // with L_sm the pre-staged group is already applied
+        const int Dpre = D > 0 ? pre_sm[0] : 0;     // slots staged during the main loop
+        const int g_begin = use_lsm ? Dpre : 0;  // with L_sm the pre-staged group is already applied
         if (a.fuse && D > g_begin) {
             T* Blate = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128) +
                        (size_t)2 * kYChunk * BM;  // after the two y buffers
             const size_t late_bytes = (size_t)stages * stage_bytes - (reinterpret_cast<uint8_t*>(Blate) - smem);
             const int dlate = max(1, static_cast<int>(late_bytes / ((size_t)BM * R * sizeof(T))));
             for (int g0 = g_begin; g0 < D;) {
-                const bool pre = g0 == 0 && a.dpre > 0;
-                const int Dg = pre ? min(D, a.dpre) : min(D - g0, dlate);
-                const T* Bg = pre ? Bpre : Blate;
+                const bool pre = g0 == 0 && Dpre > 0;
+                const int Dg = pre ? min(D, Dpre) : min(D - g0, dlate);
+                const T* Bg = Blate;
                 if (!pre) {
                     named_bar_sync(1, 128);
                     const int total = Dg * BM * chunks;
@@ -533,7 +623,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 }
                 for (int q0 = 0; q0 < cnt; q0 += 8) {
                     float acc[8];
-                    lora_batch8<T>(Bg, S_sm, dloc_sm, q0, cnt, g0, Dg, row, R, lane, acc);
+                    if (pre && a.compact)
+                        lora_batch8_pre<T>(reinterpret_cast<const uint4*>(Bpre), pre_sm, S_sm, dloc_sm, q0, cnt, Dg,
+                                           row, R, lane, acc);
+                    else
+                        lora_batch8<T>(pre ? Bpre : Bg, S_sm, dloc_sm, q0, cnt, g0, Dg, row, R, lane, acc);
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         if (q0 + u < cnt) own[(q0 + u) * BM + row] += acc[u];
@@ -834,7 +928,8 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 // ============================================================================================
 
 struct DecodePlan {
-    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre, push, s_parts, nacc, kc;
+    int n_pad, m_tiles, kb_total, splits, kb_per_split, stages, tmem_cols, dpre, push, s_parts, nacc, kc, compact;
+    size_t bpre;  // room for staged B tiles: at least dpre slots in the worst case
     size_t smem;
 };
 
@@ -860,11 +955,14 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     const int per = (p.n_pad + p.splits - 1) / p.splits;
     const size_t stage_bytes = ((size_t)BM * BK * 2 + (size_t)p.n_pad * BK * 2) * p.kc;
     const bool use_lsm = per <= kLsmMaxTokens;
-    // dedicated region: 4 int arrays, s parts [s_parts][per][R], LoRA term [per][128] (small
-    // shares), alignment, barriers
-    const size_t fixed = (size_t)per * 4 * 4 + 16 + (size_t)s_parts * per * pv.R * 4 +
-                         (use_lsm ? (size_t)per * BM * 4 : 0) + 16 + 2 * 1024;
-    const size_t slot_b = (size_t)BM * pv.R * 2;
+    // dedicated region: 4 int arrays, the staged-slot table, s parts [s_parts][per][R], LoRA
+    // term [per][128] (small shares), alignment, barriers
+    const size_t fixed = (size_t)per * 4 * 4 + (1 + 2 * kMaxPre) * 4 + 16 + (size_t)s_parts * per * pv.R * 4 +
+                         (use_lsm ? (size_t)per * BM * 4 : 0) + 128 + 2 * 1024;
+    const size_t slot_b = (size_t)BM * pv.R * 2;  // one B tile at r_max (the late path's unit)
+    // B tiles staged during the main loop are kept at their slots' true ranks: k slots need at
+    // most this many bytes (the k largest ranks among the pool's slots, empty slots at r_max)
+    auto pre_bytes = [&](int k) { return (size_t)BM * 16 * pv.top_chunks[std::min(k, kMaxPre)]; };
     const int want = std::min(std::min(per, pv.S), 32);
     const size_t limit = 225 * 1024;
     // stage area after the main loop: P [n_pad][128] + receive buffer [splits-1][per][128]
@@ -875,15 +973,22 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     p.push = 1;
     p.stages = 0;
     p.dpre = 0;
+    p.bpre = 0;
+    p.compact = 0;
     for (int pass = 0; pass < 2 && !p.stages; ++pass) {
         const size_t park = pass == 0 ? park_push : park_pull;
         int min_stages = 2;
         while ((size_t)min_stages * stage_bytes < park) ++min_stages;
         for (int st = std::max(8, min_stages); st >= std::max(p.kc == 2 ? 2 : 3, min_stages); --st) {
             if ((size_t)st * stage_bytes + fixed > limit) continue;
-            const int dp = (int)std::min<size_t>((size_t)want, (limit - st * stage_bytes - fixed) / slot_b);
+            const size_t room = limit - st * stage_bytes - fixed;
+            int dp = 0;
+            while (dp < want && pre_bytes(dp + 1) <= room) ++dp;
             p.stages = st;
             p.dpre = dp;
+            // tiles at r_max when the worst case fits that way (no rank reads in the kernel)
+            p.compact = (size_t)want * slot_b > room;
+            p.bpre = p.compact ? std::min(room, pre_bytes(want)) / 16 * 16 : std::min(room / slot_b, (size_t)want) * slot_b;
             p.push = pass == 0;
             if (dp >= want) break;
         }
@@ -895,7 +1000,7 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     int cols = 32;
     while (cols < p.n_pad * p.nacc) cols <<= 1;
     p.tmem_cols = cols;
-    p.smem = (size_t)p.stages * stage_bytes + fixed + (size_t)p.dpre * slot_b + 1024;
+    p.smem = (size_t)p.stages * stage_bytes + fixed + p.bpre + 1024;
     return p;
 }
 
@@ -973,7 +1078,8 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.fuse = fuse ? 1 : 0;
         a.bf16 = bf16;
         a.s_parts = s_parts;
-        a.dpre = p.dpre;
+        a.bpre_bytes = static_cast<int>(p.bpre);
+        a.compact = p.compact;
         a.push = p.push;
         a.prefetch = static_cast<const char*>(prefetch);
         a.prefetch_bytes = prefetch ? prefetch_bytes : 0;
@@ -983,7 +1089,12 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
                                                227 * 1024));
             attr_set = true;
         }
-        void* args[] = {(void*)&mW, (void*)&mX, (void*)&mY, (void*)&mYt, (void*)&a};
+        // B viewed as [n_slots * h_out rows][r_max / 8 chunks][8 columns]: one box = one chunk
+        // column of 128 feature rows (staging at the slots' true ranks)
+        CUtensorMap mB;
+        rc = make_map_bchunks(&mB, pv.B, bf16, pv.R, (uint64_t)pv.S * pv.h_out);
+        if (rc) return rc;
+        void* args[] = {(void*)&mW, (void*)&mX, (void*)&mY, (void*)&mYt, (void*)&mB, (void*)&a};
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(p.m_tiles, p.splits);

@@ -11,6 +11,7 @@
 // default-deny validation of "Multi-LoRA 在线服务隔离" (ai.codenodex.com), section
 // "请求身份决定适配器，而非客户端参数": an unknown or unmounted slot is an explicit error.
 #include <algorithm>
+#include <functional>
 #include <vector>
 #include <cstdio>
 #include <cstring>
@@ -62,6 +63,19 @@ PoolView pool_view(const lora_pool_t p) {
     v.R = p->desc.r_max;
     v.S = p->desc.n_slots;
     v.dtype = p->desc.dtype;
+    lora_pool* q = const_cast<lora_pool*>(p);
+    if (q->top_dirty) {
+        const int R8 = (p->desc.r_max + 7) / 8;
+        std::vector<int> c(p->desc.n_slots, R8);
+        for (int s = 0; s < p->desc.n_slots; ++s)
+            if (p->mounted[s]) c[s] = std::min(R8, (p->ranks[s] + 7) / 8);
+        const int k = std::min<int>(32, (int)c.size());
+        std::partial_sort(c.begin(), c.begin() + k, c.end(), std::greater<int>());
+        q->top_chunks[0] = 0;
+        for (int i = 1; i <= 32; ++i) q->top_chunks[i] = q->top_chunks[i - 1] + (i <= k ? c[i - 1] : 0);
+        q->top_dirty = false;
+    }
+    for (int i = 0; i <= 32; ++i) v.top_chunks[i] = p->top_chunks[i];
     return v;
 }
 
@@ -339,6 +353,7 @@ int lora_pool_create(const lora_pool_desc* desc, void* dev_mem, size_t bytes, vo
     p->A = p->base + L.A_off;
     p->B = p->base + L.B_off;
     p->mounted.assign(desc->n_slots, 0);
+    p->ranks.assign(desc->n_slots, 0);
     *out = p;
     return LORA_OK;
 }
@@ -376,6 +391,8 @@ int lora_pool_load_slot(lora_pool_t pool, int slot, const void* A_dev, const voi
     LORA_CUDA_TRY(cudaLaunchKernel(fn, dim3(blocks), dim3(threads), args, 0, st));
     count_launch();
     pool->mounted[slot] = 1;
+    pool->ranks[slot] = rank;
+    pool->top_dirty = true;
     return LORA_OK;
 }
 
@@ -422,7 +439,11 @@ int lora_pool_load_slots(lora_pool_t pool, int count, const int* slots, const vo
         void* args[] = {(void*)&b, (void*)&Ab, (void*)&Bb, (void*)&tb, (void*)&R, (void*)&hi, (void*)&ho};
         LORA_CUDA_TRY(cudaLaunchKernel(fn, dim3(per_slot, nb), dim3(256), args, 0, st));
         count_launch();
-        for (int i = 0; i < nb; ++i) pool->mounted[slots[c0 + i]] = 1;
+        for (int i = 0; i < nb; ++i) {
+            pool->mounted[slots[c0 + i]] = 1;
+            pool->ranks[slots[c0 + i]] = ranks[c0 + i];
+        }
+        pool->top_dirty = true;
     }
     return LORA_OK;
 }
@@ -433,6 +454,8 @@ int lora_pool_unload_slot(lora_pool_t pool, int slot, void* stream) {
         return set_error(LORA_ESLOT, "slot %d outside [0, %d)", slot, pool->desc.n_slots);
     LORA_CUDA_TRY(cudaMemsetAsync(static_cast<SlotEntry*>(pool->table) + slot, 0, sizeof(SlotEntry), (cudaStream_t)stream));
     pool->mounted[slot] = 0;
+    pool->ranks[slot] = 0;
+    pool->top_dirty = true;
     return LORA_OK;
 }
 

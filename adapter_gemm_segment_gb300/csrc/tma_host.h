@@ -77,5 +77,22 @@ inline int make_map_plain(CUtensorMap* m, const void* base, int bf16, uint64_t c
     return LORA_OK;
 }
 
+// A pool's B slab [rows][r_max] (16-bit) seen as [rows][r_max / 8][8]: one box is one 8-column
+// chunk of 128 consecutive rows, landing as [128][8] (16 bytes per row), no swizzle.
+inline int make_map_bchunks(CUtensorMap* m, const void* base, int bf16, uint64_t r_max, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[3] = {8, r_max / 8, rows};
+    const cuuint64_t strides[2] = {16, r_max * 2};
+    const cuuint32_t box[3] = {8u, 1u, 128u};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(LORA_ECUDA, "cuTensorMapEncodeTiled (B chunks) failed (%d)", (int)r);
+    return LORA_OK;
+}
+
 }  // namespace tc
 }  // namespace lora

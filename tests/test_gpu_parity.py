@@ -632,3 +632,46 @@ def test_cache_errors(lib):
     fresh = lib.LoraPool(128, 128, 8, S, torch.float16, DEV)
     assert code(lambda: lib.LoraCache([fresh, other])) == lib.LORA_EINVAL  # slot counts differ
     cache.close()
+
+
+# ------------------------------------------------------------------------------------------
+# B tiles staged at true ranks: a graph captured with low ranks, replayed after remounting
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", [1, 0])
+def test_graph_replay_after_remount_at_larger_ranks(lib, variant):
+    """The decode GEMM sizes its staging of B tiles from the ranks mounted when it is
+    launched; a CUDA graph keeps that launch.  After slots are remounted at r_max the replay
+    must still be exact (tiles that no longer fit take the late path)."""
+    n, h, R = 64, 4096, 64
+    low = wl.random_case(80, n, h, 512, [8, 8, 16, 16, 8, 8], r_max=R, dtype=torch.float16, p_base=0.0)
+    high = wl.random_case(81, n, h, 512, [64, 64, 64, 64, 64, 64], r_max=R, dtype=torch.float16,
+                          idx=low.idx.numpy())
+    pool = make_pool(lib, low)
+    seg = pool.segment(low.idx.to(DEV))
+    W, x = low.W.to(DEV), low.x.to(DEV)
+    y = torch.empty(n, 512, dtype=torch.float16, device=DEV)
+    ws = pool.linear_workspace(n)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        lib.lora_linear_fwd(pool.handle, W, x, y, seg, ws, variant)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        lib.lora_linear_fwd(pool.handle, W, x, y, seg, ws, variant)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_parity(y.cpu(), O.lora_linear_case(low), "graph, low ranks")
+    for s in range(6):  # same slots, now at r_max (on the capture stream, ordered before the replay)
+        pool.unload_slot(s, stream=st)
+        pool.load_slot(s, high.adapters.A[s].to(DEV), high.adapters.B[s].to(DEV), high.adapters.alphas[s], stream=st)
+    with torch.cuda.stream(st):
+        g.replay()
+    torch.cuda.synchronize()
+    want = O.lora_linear(low.x, low.W, O.pool_of_case(high), low.idx.numpy())
+    assert_parity(y.cpu(), want, "graph replayed after remounting at r_max")
+    y0 = torch.empty_like(y)
+    lib.lora_linear_fwd(pool.handle, torch.zeros_like(W), x, y0, seg, ws, variant)
+    torch.cuda.synchronize()
+    assert_lora_only_parity(y0.cpu(), O.lora_linear(low.x, torch.zeros_like(low.W), O.pool_of_case(high),
+                                                    low.idx.numpy()), "remounted, W=0")
