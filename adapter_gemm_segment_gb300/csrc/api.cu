@@ -246,9 +246,11 @@ int lora_linear_group_policy(int count, const lora_pool_t* pools, int n_tokens, 
     GroupView grp;
     const int rc = group_setup(count, pools, pvs, &grp);
     if (rc) return rc;
-    // Measured on GB300 (7B-shaped layers, 64 and 256 tokens, bf16, r_max 16): the base GEMM
-    // over the concatenated weight plus one segmented expand beat per-slice fused GEMMs at
-    // decode sizes; prefill batches keep the fused epilogue.
+    // A group of one is a single linear: its policy.  Otherwise, measured on GB300 (7B-shaped
+    // layers, 64 and 256 tokens, bf16, r_max 16): the base GEMM over the concatenated weight
+    // plus one segmented expand beat per-slice fused GEMMs at decode sizes; prefill batches
+    // keep the fused epilogue.
+    if (count == 1) return lora_linear_policy(pools[0], n_tokens, variant);
     *variant = n_tokens <= 256 ? LORA_VARIANT_SEPARATE : LORA_VARIANT_FUSED;
     return LORA_OK;
 }

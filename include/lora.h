@@ -99,6 +99,8 @@ typedef struct lora_pool* lora_pool_t;
  *   idx_dev           copy of the batch's idx (original order)               [n]
  *   items_dev         shrink work items: every adapter segment cut into runs of up to 4
  *                     sorted tokens, {slot, count, token[4], rank, 0} each   [n][8]
+ *                     (rank: the slot's rank in the pool the segments were built on, a
+ *                     hint -- kernels of another pool check their own slot table) 
  * Segments are rebuilt once per batch and reused by every linear layer that runs
  * over that batch, as long as the workspace stays alive and unmodified. */
 typedef struct {
@@ -248,9 +250,10 @@ int lora_linear_policy(lora_pool_t pool, int n_tokens, int* variant);
 int lora_linear_group_workspace_bytes(int count, const lora_pool_t* pools, int n_tokens, size_t* bytes);
 int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev, const void* x_dev, void* y_dev,
                           const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes, void* stream);
-/* Which variant AUTO picks for a group (1 or 2): separate -- one base GEMM over the
- * concatenated weight, then one segmented expand over every slice -- for batches of up to
- * 256 tokens, fused above.  Measured on GB300; host-only. */
+/* Which variant AUTO picks for a group (1 or 2): for one slice, lora_linear_policy's choice;
+ * otherwise separate -- one base GEMM over the concatenated weight, then one segmented expand
+ * over every slice -- for batches of up to 256 tokens, fused above.  Measured on GB300;
+ * host-only. */
 int lora_linear_group_policy(int count, const lora_pool_t* pools, int n_tokens, int* variant);
 
 /* ---- host-tier adapter cache -------------------------------------------------------------

@@ -505,6 +505,8 @@ def test_group_errors(lib):
     assert torch.count_nonzero(y) == 0  # nothing ran
     assert lib.lora_linear_group_policy(handles, 64) == lib.LORA_VARIANT_SEPARATE
     assert lib.lora_linear_group_policy(handles, 4096) == lib.LORA_VARIANT_FUSED
+    for n in (1, 64, 256, 4096):  # a group of one follows the single-linear policy
+        assert lib.lora_linear_group_policy(handles[:1], n) == lib.lora_linear_policy(handles[0], n)
 
 
 @pytest.mark.parametrize("n", [16, 300])
