@@ -158,8 +158,9 @@ pool_load_batch_kernel(const __grid_constant__ LoadBatch b, char* __restrict__ A
 }
 
 // ---- segment builder -----------------------------------------------------------------------
-// One CTA of 1024 threads.  Shared memory: cnt[K], off[K], wcnt[32][K] (uint16) with
-// K = S + 1 keys (key k+1 for slot k, key 0 for idx -1).
+// One CTA of 1024 threads.  Shared memory: cnt[K], off[K], rk[K], wcnt[32][K] (uint16) with
+// K = S + 1 keys (key k+1 for slot k, key 0 for idx -1); rk[k] = rank of the slot of key k if
+// it is mounted, else 0 (copied from the slot table once, so no token waits on a table read).
 constexpr int kSegThreads = 1024;
 constexpr int kItemTok = 4;  // sorted tokens per shrink work item
 
@@ -172,23 +173,36 @@ segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restri
     const int K = S + 1;
     int* cnt = smem_i;
     int* off = cnt + K;
-    uint16_t* wcnt = reinterpret_cast<uint16_t*>(off + K);
+    int* rk = off + K;
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(rk + K);
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int U = 4;  // tokens per thread whose loads are issued together
 
-    pdl_wait();  // idx may come from the previous kernel in the stream
-    for (int i = tid; i < K; i += kSegThreads) cnt[i] = 0;
+    pdl_wait();  // idx and the slot table may come from earlier kernels in the stream
+    for (int i = tid; i < K; i += kSegThreads) {
+        cnt[i] = 0;
+        const SlotEntry e = i > 0 ? table[i - 1] : SlotEntry{0, 0, 0.f, 0};
+        rk[i] = (i > 0 && e.state == kSlotReady) ? max(e.rank, 1) : 0;
+    }
     for (int i = tid; i < 32 * K; i += kSegThreads) wcnt[i] = 0;
     if (tid == 0) bad = 0;
     __syncthreads();
 
     // 1. validate + histogram
-    for (int t = tid; t < n; t += kSegThreads) {
-        const int k = idx[t];
-        idx_copy[t] = k;
-        const bool ok = (k >= -1) && (k < S) && (k < 0 || table[k].state == kSlotReady);
-        if (!ok) bad = 1;
-        else atomicAdd(&cnt[k + 1], 1);
+    for (int t0 = tid; t0 < n; t0 += U * kSegThreads) {
+        int kk[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) kk[u] = t0 + u * kSegThreads < n ? idx[t0 + u * kSegThreads] : -1;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u * kSegThreads, k = kk[u];
+            if (t >= n) continue;
+            idx_copy[t] = k;
+            const bool ok = (k >= -1) && (k < S) && (k < 0 || rk[k + 1] > 0);
+            if (!ok) bad = 1;
+            else atomicAdd(&cnt[k + 1], 1);
+        }
     }
     __syncthreads();
     if (bad) {
@@ -277,20 +291,34 @@ segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restri
         if (lane == 0) nseg_out[1] = run;
     }
     __syncthreads();
-    for (int j = tid; j < n; j += kSegThreads) {
-        const int t = perm[j];
-        const int key = idx[t] + 1;
-        if (key == 0) continue;
-        const int rel = j - (off[key] - cnt[key]);
-        int32_t* it = items + (size_t)(ibase[key] + rel / kItemTok) * 8;
-        it[2 + rel % kItemTok] = t;
-        if (rel % kItemTok == 0) {
-            const int nt = min(kItemTok, cnt[key] - rel);
-            it[0] = key - 1;
-            it[1] = nt;
-            for (int u = nt; u < kItemTok; ++u) it[2 + u] = t;  // padding: a valid token
-            it[6] = table[key - 1].rank;                          // the adapter's true rank
-            it[7] = 0;
+    for (int j0 = tid; j0 < n; j0 += U * kSegThreads) {
+        int tt[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) tt[u] = j0 + u * kSegThreads < n ? perm[j0 + u * kSegThreads] : 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * kSegThreads, t = tt[u];
+            if (j >= n) continue;
+            // the key of sorted position j: the first key whose range ends past j
+            int lo = 0, hi = K - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (off[mid] > j) hi = mid;
+                else lo = mid + 1;
+            }
+            const int key = lo;
+            if (key == 0) continue;
+            const int rel = j - (off[key] - cnt[key]);
+            int32_t* it = items + (size_t)(ibase[key] + rel / kItemTok) * 8;
+            it[2 + rel % kItemTok] = t;
+            if (rel % kItemTok == 0) {
+                const int nt = min(kItemTok, cnt[key] - rel);
+                it[0] = key - 1;
+                it[1] = nt;
+                for (int v = nt; v < kItemTok; ++v) it[2 + v] = t;  // padding: a valid token
+                it[6] = rk[key];                                      // the adapter's true rank
+                it[7] = 0;
+            }
         }
     }
     pdl_trigger();
@@ -488,11 +516,11 @@ int lora_segment(const int32_t* idx_dev, int n_tokens, lora_pool_t pool, void* w
     out->n_slots = S;
 
     const int K = S + 1;
-    const size_t smem = sizeof(int) * 2 * (size_t)K + sizeof(uint16_t) * 32 * (size_t)K;
+    const size_t smem = sizeof(int) * 3 * (size_t)K + sizeof(uint16_t) * 32 * (size_t)K;
     static bool attr_set = false;  // one device per process is the supported configuration
     if (!attr_set) {
         LORA_CUDA_TRY(cudaFuncSetAttribute(segment_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)(sizeof(int) * 2 * (kMaxSlots + 1) +
+                                           (int)(sizeof(int) * 3 * (kMaxSlots + 1) +
                                                  sizeof(uint16_t) * 32 * (kMaxSlots + 1))));
         attr_set = true;
     }
