@@ -328,6 +328,10 @@ int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev
                                 0, &gq);
             if (rc) return rc;
         }
+    } else if (decode && !fused && count > 1 && n > 64) {
+        // x is as large as the W tiles here: 256-row tiles halve its re-reads
+        rc = launch_gemm_tall(pcat, sv, W_dev, x_dev, y_dev, grp.ldy, st);
+        if (rc) return rc;
     } else {
         // one base GEMM over the concatenated weight; the prefill kernel applies each slice's
         // LoRA term in its epilogue

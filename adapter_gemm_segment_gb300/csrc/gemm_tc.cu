@@ -924,6 +924,135 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 }
 
 // ============================================================================================
+// tall-tile base GEMM (no LoRA term) for grouped batches of 128-256 tokens
+// ============================================================================================
+// At 128-256 tokens the x tile of a stage is as large as the W tile or larger, and every row
+// tile re-reads all of x.  Here a CTA owns 256 W rows: each K stage brings a [256 rows][64] W
+// box and one x box, and two M=128 MMAs (rows 0-127 and 128-255, accumulators in TMEM columns
+// [0, n_pad) and [n_pad, 2 n_pad)) read the same x tile, so x is re-read half as often.  Full
+// K per CTA, no split, no LoRA epilogue (the segmented expand follows); y stored directly.
+struct TallArgs {
+    SegView seg;
+    void* y;
+    int n, n_pad, ldy, h_out, nkb, stages, bf16;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tall_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const TallArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_align(smem_raw, 1024);
+    const int stages = a.stages;
+    const uint32_t w_bytes = 2 * BM * BK * 2;  // 256 rows
+    const uint32_t stage_bytes = w_bytes + static_cast<uint32_t>(a.n_pad) * BK * 2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * stage_bytes);
+    uint64_t* empty = full + stages;
+    uint64_t* acc_full = empty + stages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * 2 * BM;  // first W row of this CTA
+    int cols = 32;
+    while (cols < 2 * a.n_pad) cols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        flags[0] = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+
+    if (warp == 0) {
+        // W and x are complete when this grid starts: the shrink before it releases its
+        // dependents only after its own grid-dependency wait
+        if (lane == 0) {
+            int it = 0;
+            for (; it < a.nkb && !flags[0]; ++it) {
+                const int s = it % stages;
+                if (it >= stages && !mbar_wait(&empty[s], ((it / stages) & 1) ^ 1, flags)) break;
+                mbar_arrive_expect_tx(&full[s], stage_bytes);
+                tma_load_2d_cta(smem + (size_t)s * stage_bytes, &tmW, &full[s], it * BK, m0);
+                tma_load_2d_cta(smem + (size_t)s * stage_bytes + w_bytes, &tmX, &full[s], it * BK, 0);
+            }
+            if (flags[0]) {  // aborted: let copies already in flight land before the CTA exits
+                report_timeout_status(a.seg.status);
+                for (int i = max(0, it - stages); i < it; ++i) {
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BM, a.n_pad, a.bf16 != 0);
+            for (int i = 0; i < a.nkb; ++i) {
+                const int s = i % stages;
+                if (!mbar_wait(&full[s], (i / stages) & 1, flags)) {
+                    report_timeout_status(a.seg.status);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t wa = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint32_t xa = wa + w_bytes;
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k) {
+                    const uint64_t xd = sdesc_sw128(xa + k * UMMA_K * 2);
+                    const uint32_t acc_flag = (i > 0 || k > 0) ? 1u : 0u;
+                    umma_f16(tmem, sdesc_sw128(wa + k * UMMA_K * 2), xd, idesc, acc_flag);
+                    umma_f16(tmem + static_cast<uint32_t>(a.n_pad), sdesc_sw128(wa + BM * 128 + k * UMMA_K * 2), xd,
+                             idesc, acc_flag);
+                }
+                umma_commit(&empty[s]);
+            }
+            umma_commit(acc_full);  // also on abort: fires once the issued MMAs have finished
+        }
+    } else {
+        // ---- epilogue: thread <-> W row r of each 128-row half (TMEM lane) ----
+        const int row = (warp & 3) * 32 + lane;
+        T* y = static_cast<T*>(a.y);
+        pdl_wait();  // the status word comes from an earlier kernel
+        const bool st_ok = __ldcg(a.seg.status) == LORA_OK;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, flags));
+        if (got && st_ok) {
+            tc_fence_after();
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t taddr =
+                    tmem + static_cast<uint32_t>(h * a.n_pad) + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+                const int o = m0 + h * BM + row;
+                for (int t0 = 0; t0 < a.n_pad; t0 += 16) {
+                    uint32_t r[16];
+                    __syncwarp();
+                    tmem_ld16(taddr + t0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (o < a.h_out && t0 + q < a.n) y[(size_t)(t0 + q) * a.ldy + o] = from_f32<T>(__uint_as_float(r[q]));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, cols);
+}
+
+// ============================================================================================
 // host side
 // ============================================================================================
 
@@ -1148,6 +1277,48 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     void* args[] = {(void*)&mX, (void*)&mW, (void*)&a};
     LORA_CUDA_TRY(launch_pdl((const void*)gemm_prefill_kernel<T>, dim3(grid), dim3(kThreads), smem, st, args));
     return LORA_OK;
+}
+
+template <typename T>
+static int launch_tall_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, void* y, int ldy,
+                         cudaStream_t st) {
+    using namespace tc;
+    const int n = sv.n;
+    if (n == 0) return LORA_OK;
+    if (n > kDecodeMaxN) return set_error(LORA_EINVAL, "internal: tall-tile GEMM for more than 256 tokens");
+    TallArgs a;
+    a.seg = sv;
+    a.y = y;
+    a.n = n;
+    a.n_pad = std::max(16, (n + 15) / 16 * 16);
+    a.ldy = ldy;
+    a.h_out = pv.h_out;
+    a.nkb = (pv.h_in + BK - 1) / BK;
+    a.bf16 = pv.dtype == LORA_BF16;
+    const size_t stage_bytes = (size_t)2 * BM * BK * 2 + (size_t)a.n_pad * BK * 2;
+    a.stages = std::max(2, std::min(6, (int)(kSmemBudget / stage_bytes)));
+    const size_t smem = (size_t)a.stages * stage_bytes + (2 * (size_t)a.stages + 1) * 8 + 16 + 1024;
+    CUtensorMap mW, mX;
+    int rc = make_map(&mW, W, a.bf16, pv.h_in, pv.h_out, 2 * BM);
+    if (rc) return rc;
+    rc = make_map(&mX, x, a.bf16, pv.h_in, n, a.n_pad);
+    if (rc) return rc;
+    static bool attr_set = false;
+    if (!attr_set) {
+        LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_tall_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           227 * 1024));
+        attr_set = true;
+    }
+    void* args[] = {(void*)&mW, (void*)&mX, (void*)&a};
+    LORA_CUDA_TRY(launch_pdl((const void*)gemm_tall_kernel<T>, dim3((pv.h_out + 2 * BM - 1) / (2 * BM)), dim3(kThreads),
+                             smem, st, args));
+    return LORA_OK;
+}
+
+int launch_gemm_tall(const PoolView& pv, const SegView& sv, const void* W, const void* x, void* y, int ldy,
+                     cudaStream_t st) {
+    if (pv.dtype == LORA_F16) return launch_tall_t<__half>(pv, sv, W, x, y, ldy, st);
+    return launch_tall_t<__nv_bfloat16>(pv, sv, W, x, y, ldy, st);
 }
 
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,

@@ -49,6 +49,11 @@ int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const v
                    void* y, bool fuse, cudaStream_t st, const void* prefetch = nullptr, size_t prefetch_bytes = 0,
                    const GroupView* grp = nullptr);
 
+// Base GEMM y = x W^T (no LoRA term) with 256 W rows per CTA, two M=128 MMAs sharing each x
+// tile, full K per CTA (batches of up to 256 tokens); y has row stride ldy.
+int launch_gemm_tall(const PoolView& pv, const SegView& sv, const void* W, const void* x, void* y, int ldy,
+                     cudaStream_t st);
+
 // Grouped tcgen05 shrink for batches of more than 256 tokens (one CTA per 128-token tile).
 int shrink_tc_supported(const PoolView& pv);
 int launch_shrink_tc(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st);
