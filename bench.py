@@ -533,7 +533,8 @@ def ours(args):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": read_profile_traffic(f"gemm_decode_{args.workload}"),
-                "kernel": "gemm_decode_kernel", "kernel_ms": gemm_ms,
+                "kernel": ("base GEMM calls: gemm_tall_kernel (grouped q|k|v, gate|up), gemm_decode_kernel (o, down)"
+                           if args.workload == "layer" and grouped else "gemm_decode_kernel"), "kernel_ms": gemm_ms,
                 "algorithmic_bytes_per_launch": sum(a_["gemm_bytes"] for a_ in algs) / n_lin,
                 "peak_source": peaks["source"] + " copy"}
     roof["shrink_ms"] = shrink_ms
