@@ -89,7 +89,7 @@ struct GroupView {
     int count;
     int ldy;
     int col[kMaxGroup + 1];
-    int blk[kMaxGroup + 1];  // first 256-feature block of each slice (segmented expand grid)
+    int blk[kMaxGroup + 1];  // first expand block of each slice (set by the expand launcher)
     const SlotEntry* table[kMaxGroup];
     const void* A[kMaxGroup];
     const void* B[kMaxGroup];
