@@ -216,6 +216,7 @@ static int group_setup(int count, const lora_pool_t* pools, PoolView* pvs, Group
         grp->table[q] = p.table;
         grp->A[q] = p.A;
         grp->B[q] = p.B;
+        grp->rank_aware |= has_padded_slots(p);
         grp->col[q + 1] = grp->col[q] + p.h_out;
         grp->blk[q + 1] = grp->blk[q] + (p.h_out + 255) / 256;
     }
@@ -322,6 +323,7 @@ int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev
             gq.table[0] = pvs[q].table;
             gq.A[0] = pvs[q].A;
             gq.B[0] = pvs[q].B;
+            gq.rank_aware = has_padded_slots(pvs[q]);
             const char* Wq = static_cast<const char*>(W_dev) + (size_t)grp.col[q] * p0.h_in * elt;
             char* yq = static_cast<char*>(y_dev) + (size_t)grp.col[q] * elt;
             rc = launch_gemm_tc(pvs[q], sv, Wq, x_dev, s_buf + (size_t)q * grp.s_stride, s_parts, yq, true, st, nullptr,

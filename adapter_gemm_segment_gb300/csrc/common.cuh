@@ -94,7 +94,15 @@ struct GroupView {
     const void* A[kMaxGroup];
     const void* B[kMaxGroup];
     long long s_stride;  // floats between the shrink outputs of consecutive slices
+    int rank_aware;      // some mounted slot holds a rank below r_max: kernels may skip its padding
 };
+
+// Whether some slot of the pool (empty slots count at r_max) holds fewer 8-column chunks than
+// r_max: then skipping a slot's padding saves reads.
+inline int has_padded_slots(const PoolView& pv) {
+    const int k = pv.S < 32 ? pv.S : 32;
+    return pv.top_chunks[k] < k * ((pv.R + 7) / 8) ? 1 : 0;
+}
 
 inline GroupView single_group(const PoolView& pv) {
     GroupView g;
@@ -106,6 +114,7 @@ inline GroupView single_group(const PoolView& pv) {
     g.table[0] = pv.table;
     g.A[0] = pv.A;
     g.B[0] = pv.B;
+    g.rank_aware = has_padded_slots(pv);
     return g;
 }
 

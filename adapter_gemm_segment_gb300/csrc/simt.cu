@@ -446,10 +446,13 @@ expand_seg_kernel(PoolView pool, GroupView grp, SegView seg, const float* __rest
     __syncthreads();
     if (!live0) return;
     const T* Br = static_cast<const T*>(sl.B) + ((size_t)slot * h_out + o) * R;
+    // columns past the adapter's true rank are zero in B (and in s): skip them when the pool
+    // has padded slots (the rank comes from this pool's own table)
+    const int jmax = grp.rank_aware ? min(R, (max(sl.table[slot].rank, 1) + 7) & ~7) : R;
     float acc[2][kItemTok];
 #pragma unroll
     for (int u = 0; u < kItemTok; ++u) acc[0][u] = acc[1][u] = 0.f;
-    for (int j = 0; j < R; j += 8) {
+    for (int j = 0; j < jmax; j += 8) {
         float b0[8], b1[8];
         unpack8<T>(__ldg(reinterpret_cast<const uint4*>(Br + j)), b0);
         unpack8<T>(live1 ? __ldg(reinterpret_cast<const uint4*>(Br + (size_t)256 * R + j)) : make_uint4(0, 0, 0, 0), b1);
