@@ -433,6 +433,9 @@ GROUPS = [
     (50, 500, 256, [256, 128, 128], [8, 4, 8, 8, 1], 8, torch.float16),
     (51, 300, 256, [128, 128, 128], [16] * 20, 16, torch.bfloat16),
     (52, 300, 256, [128, 256, 128], [128, 96], 128, torch.float16),
+    # the 256-row-tile GEMM just above its switch (65 tokens: N = 80), a ragged last tile
+    # (528 rows) and 5 K blocks
+    (53, 65, 320, [256, 272], [8, 16, 16], 16, torch.bfloat16),
 ]
 
 
