@@ -436,6 +436,9 @@ GROUPS = [
     # the 256-row-tile GEMM just above its switch (65 tokens: N = 80), a ragged last tile
     # (528 rows) and 5 K blocks
     (53, 65, 320, [256, 272], [8, 16, 16], 16, torch.bfloat16),
+    # the 256-row-tile GEMM with a single K block, and with 80 tiles (20480 rows)
+    (54, 100, 64, [128, 256], [8, 8], 8, torch.float16),
+    (55, 80, 128, [10240, 10240], [8, 8], 8, torch.bfloat16),
 ]
 
 
