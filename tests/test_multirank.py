@@ -74,3 +74,29 @@ def test_profile_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench.read_profile_traffic("gemm_decode_decode") == 35937024.0
     assert bench.read_profile_traffic("gemm_prefill_prefill") is None  # taken on another source
     assert bench.read_profile_traffic("no_such_profile") is None
+
+
+def test_algorithmic_bytes_and_flops_hand_worked():
+    # 6 tokens, idx [-1, 0, 0, 2, -1, 5]: D = 3 distinct adapters, n_L = 4 LoRA tokens;
+    # h_in 10, h_out 7, r_max 4, 2-byte elements
+    a = bench.algorithmic_case([-1, 0, 0, 2, -1, 5], 10, 7, 4)
+    assert (a["D"], a["n_L"]) == (3, 4)
+    W, A_D, B_D, xy = 7 * 10 * 2, 3 * 4 * 10 * 2, 3 * 7 * 4 * 2, 6 * (10 + 7) * 2
+    assert a["linear_bytes"] == W + A_D + B_D + xy == 752
+    assert a["gemm_bytes"] == W + B_D + xy == 512
+    assert a["linear_flops"] == 2 * 6 * 10 * 7 + 2 * 4 * 4 * (10 + 7) == 1384
+    assert a["gemm_flops"] == 2 * 6 * 10 * 7 + 2 * 4 * 4 * 7 == 1064
+
+
+def test_algorithmic_bytes_match_the_decode_figure():
+    # decode q_proj: 64 tokens, 4096 x 4096 fp16, r_max 8, 27 adapters touched:
+    # 33.55 MB of W + 3.54 MB of adapters + 1.05 MB of x and y
+    idx = [k % 27 for k in range(64)]
+    a = bench.algorithmic_case(idx, 4096, 4096, 8)
+    assert a["D"] == 27 and a["n_L"] == 64
+    assert abs(a["linear_bytes"] / 1e6 - (33.554 + 3.539 + 1.049)) < 0.01
+
+
+def test_job_throughput_counts_every_rank():
+    assert bench.job_tokens_per_s(1, 1000, 10, 5.0) == 1000 * 10 / 5e-3
+    assert bench.job_tokens_per_s(4, 1000, 10, 5.0) == 4 * 1000 * 10 / 5e-3
