@@ -935,6 +935,7 @@ struct TallArgs {
     SegView seg;
     void* y;
     int n, n_pad, ldy, h_out, nkb, stages, bf16;
+    int tstep;  // tokens per CTA (grid.y splits the batch when the row tiles fill few SMs)
 };
 
 template <typename T>
@@ -953,6 +954,7 @@ gemm_tall_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * 2 * BM;  // first W row of this CTA
+    const int ts = blockIdx.y * a.tstep;  // first token of this CTA
     int cols = 32;
     while (cols < 2 * a.n_pad) cols <<= 1;
 
@@ -987,7 +989,7 @@ gemm_tall_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 if (it >= stages && !mbar_wait(&empty[s], ((it / stages) & 1) ^ 1, flags)) break;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tma_load_2d_cta(smem + (size_t)s * stage_bytes, &tmW, &full[s], it * BK, m0);
-                tma_load_2d_cta(smem + (size_t)s * stage_bytes + w_bytes, &tmX, &full[s], it * BK, 0);
+                tma_load_2d_cta(smem + (size_t)s * stage_bytes + w_bytes, &tmX, &full[s], it * BK, ts);
             }
             if (flags[0]) {  // aborted: let copies already in flight land before the CTA exits
                 report_timeout_status(a.seg.status);
@@ -1042,7 +1044,8 @@ gemm_tall_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                     tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
-                        if (o < a.h_out && t0 + q < a.n) y[(size_t)(t0 + q) * a.ldy + o] = from_f32<T>(__uint_as_float(r[q]));
+                        if (o < a.h_out && t0 + q < a.tstep && ts + t0 + q < a.n)
+                            y[(size_t)(ts + t0 + q) * a.ldy + o] = from_f32<T>(__uint_as_float(r[q]));
                 }
             }
         }
@@ -1290,7 +1293,12 @@ static int launch_tall_t(const PoolView& pv, const SegView& sv, const void* W, c
     a.seg = sv;
     a.y = y;
     a.n = n;
-    a.n_pad = std::max(16, (n + 15) / 16 * 16);
+    // two token halves per row tile when that still fits the SMs (q|k|v: 48 tiles -> 96 CTAs);
+    // each CTA then takes in W and half of x, and writes its own tokens of y
+    const int tiles = (pv.h_out + 2 * BM - 1) / (2 * BM);
+    const int tsplit = (n > 128 && 2 * tiles <= num_sms()) ? 2 : 1;
+    a.tstep = (n + tsplit - 1) / tsplit;
+    a.n_pad = std::max(16, (a.tstep + 15) / 16 * 16);
     a.ldy = ldy;
     a.h_out = pv.h_out;
     a.nkb = (pv.h_in + BK - 1) / BK;
@@ -1310,8 +1318,7 @@ static int launch_tall_t(const PoolView& pv, const SegView& sv, const void* W, c
         attr_set = true;
     }
     void* args[] = {(void*)&mW, (void*)&mX, (void*)&a};
-    LORA_CUDA_TRY(launch_pdl((const void*)gemm_tall_kernel<T>, dim3((pv.h_out + 2 * BM - 1) / (2 * BM)), dim3(kThreads),
-                             smem, st, args));
+    LORA_CUDA_TRY(launch_pdl((const void*)gemm_tall_kernel<T>, dim3(tiles, tsplit), dim3(kThreads), smem, st, args));
     return LORA_OK;
 }
 
