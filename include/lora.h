@@ -280,7 +280,9 @@ int lora_linear_group_policy(int count, const lora_pool_t* pools, int n_tokens, 
  *     enqueued earlier still read the evicted adapter; work on other streams must be ordered
  *     by the caller.  *mounts_out (may be NULL) = adapters mounted by this call.
  *     An unregistered id is LORA_EIDX and more distinct ids than slots is LORA_ENOSPACE;
- *     either way nothing changes and idx_out is not written.
+ *     either way nothing changes and idx_out is not written.  If a mount or unmount fails to
+ *     enqueue (LORA_ECUDA), the cache's record may no longer match the pools: destroy the
+ *     cache and its pools' contents (recreate the pools) before further use.
  *   lora_cache_unregister: forgets the adapter, unmounting it (on `stream`) if resident.
  *   lora_cache_slot_of: the slot holding adapter id, or -1 if it is not resident.
  *   lora_cache_stats: hits and misses (per distinct adapter per map call), evictions. */
