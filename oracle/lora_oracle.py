@@ -35,10 +35,16 @@ What it computes, in float64, straight from the definitions:
 
 * ``lora_linear_group``: projections sharing x and idx, side by side (see its docstring).
 
-Pins (tests/test_oracle_pins.py): brute force in pure-Python loops on tiny inputs,
-numpy's stable argsort for the segment order, the merged-weight identity, zero-pad
-invariance, permutation equivariance, the unit-vector selector closed form, the
-rank-1 outer product, and a hand-worked golden example in tests/golden/.
+* ``within_tolerance``: the elementwise float bar |y - y_ref| <= 1e-2 + 1e-2 |y_ref|.
+
+Arithmetic: float64 throughout; the base term and the per-token shrink/expand products use
+numpy's matmul (a library primitive) with no blocking or reordering of its own.
+
+Pins (tests/test_oracle_pins.py): brute force in pure-Python loops on tiny inputs (full
+batches and ``rows=`` subsets in any order), numpy's stable argsort for the segment order,
+the merged-weight identity, zero-pad invariance, permutation equivariance, the unit-vector
+selector closed form, the rank-1 outer product, hand-computed pairs on both sides of the
+tolerance bound, and a hand-worked golden example in tests/golden/.
 """
 from __future__ import annotations
 

@@ -269,9 +269,57 @@ def pin_group_errors(O):
     return False, "slot missing from one slice accepted"
 
 
+def pin_rows_subset(O):
+    """lora_linear(..., rows=r) against brute force on the requested rows, in the order given:
+    permuted, repeated and unsorted subsets, with x as a numpy array and as a torch tensor."""
+    import torch
+
+    for seed in range(3):
+        x, W, adapters, idx, r_max = tiny_problem(40 + seed, n=9, p_base=0.2)
+        pool = make_pool(O, adapters, r_max, x.shape[1], W.shape[0])
+        full = np.array(brute_force(x.tolist(), W.tolist(), adapters, idx.tolist(), r_max))
+        subsets = [[8, 0, 3], [2, 2, 7, 2], list(np.random.default_rng(seed).permutation(9)), [5]]
+        for rows in subsets:
+            for xin in (x, torch.from_numpy(x)):
+                y = O.lora_linear(xin, W, pool, idx, rows=rows)
+                if y.shape != (len(rows), W.shape[0]) or not np.allclose(y, full[rows], rtol=1e-12, atol=1e-12):
+                    return False, f"seed {seed}: rows={rows} ({type(xin).__name__} x) differ from brute force"
+    return True, ""
+
+
+def pin_tolerance(O):
+    """within_tolerance is the stated bar |y - y_ref| <= 1e-2 + 1e-2 |y_ref|, elementwise.
+    Hand-computed pairs just inside and just outside the bound (positive, negative and zero
+    references) and 16-bit outputs whose exact values are known."""
+    import torch
+
+    # (y, y_ref, expected): bound = 0.01 + 0.01 |y_ref|
+    pairs = [
+        (2.0299, 2.0, True), (2.0301, 2.0, False), (1.9701, 2.0, True), (1.9699, 2.0, False),  # bound 0.03
+        (-3.0399, -3.0, True), (-3.0401, -3.0, False), (-2.9601, -3.0, True), (-2.9599, -3.0, False),  # 0.04
+        (0.0099, 0.0, True), (-0.0101, 0.0, False),  # bound 0.01 at a zero reference
+        (100.0, 101.0, True), (98.97, 101.0, False),  # bound 1.02
+    ]
+    y = np.array([p[0] for p in pairs])
+    ref = np.array([p[1] for p in pairs])
+    got = O.within_tolerance(y, ref)
+    want = np.array([p[2] for p in pairs])
+    if got.shape != want.shape or not np.array_equal(got, want):
+        return False, f"float64 pairs: got {got.tolist()}"
+    # 16-bit inputs are upcast exactly: fp16 1 + 2^-7 vs 1.0 (diff 0.0078125 <= 0.02: inside);
+    # bf16 1 + 2^-6 vs 0.99 (diff 0.025625 > 0.0199: outside); bf16 -2^-7 vs 0 (0.0078125: inside)
+    y16 = torch.tensor([[1.0078125, 0.0]], dtype=torch.float16)
+    yb = torch.tensor([[1.015625, -0.0078125]], dtype=torch.bfloat16)
+    g16 = O.within_tolerance(y16, np.array([[1.0, 0.0]]))
+    gb = O.within_tolerance(yb, np.array([[0.99, 0.0]]))
+    if g16.tolist() != [[True, True]] or gb.tolist() != [[False, True]]:
+        return False, f"16-bit inputs: {g16.tolist()} {gb.tolist()}"
+    return True, ""
+
+
 PINS = [pin_golden, pin_brute_force, pin_segments_argsort, pin_base_only, pin_merged_weight,
         pin_zero_pad, pin_permutation, pin_selector, pin_rank1, pin_errors, pin_group_block_diagonal,
-        pin_group_brute_force, pin_group_errors]
+        pin_group_brute_force, pin_group_errors, pin_rows_subset, pin_tolerance]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -305,6 +353,11 @@ MUTANTS = {
                                 "[lora_linear(x, W, p, idx, rows=rows) for W, p in zip(Ws, pools)][::-1]"),
     "group_one_pool_for_all": ("[lora_linear(x, W, p, idx, rows=rows) for W, p in zip(Ws, pools)]",
                                "[lora_linear(x, W, pools[0], idx, rows=rows) for W, p in zip(Ws, pools)]"),
+    "rows_slot_of_output_position": ("s = int(idx[t])", "s = int(idx[i])"),
+    "rows_ignored_for_x": ("xs = _f64(x)[rows]", "xs = _f64(x)[np.sort(rows)]"),
+    "tolerance_atol_times_10": ("<= atol + rtol * np.abs(y_ref)", "<= 10 * atol + rtol * np.abs(y_ref)"),
+    "tolerance_signed_reference": ("<= atol + rtol * np.abs(y_ref)", "<= atol + rtol * y_ref"),
+    "tolerance_one_sided": ("return np.abs(y - y_ref) <=", "return (y - y_ref) <="),
 }
 
 
