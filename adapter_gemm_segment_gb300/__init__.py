@@ -2,8 +2,10 @@
 
 Argument marshalling only: every step of the path runs in the CUDA library
 ``_lib/liblora_gb300.so``.  PyTorch supplies device memory and streams.  There is no
-CPU or PyTorch fallback: if the library is missing or fails to load, importing this
-package raises.
+CPU or PyTorch fallback: the library is mapped on the first call into it (or by
+``load_library()``), and if it is missing or fails to load, that call raises ImportError.
+Importing the package alone maps nothing, so host-only users of the package (the seeded
+input generators in ``workloads``) do not load the CUDA library.
 
 Same names as the C ABI (the ``EXPORTED`` tuple: pool, segment, linear, grouped-linear and
 host-tier cache entry points), plus small ``LoraPool`` and ``LoraCache`` convenience wrappers;
@@ -100,7 +102,24 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-_lib = _load()
+class _LazyLibrary:
+    """The CDLL, mapped on first attribute access; a missing library raises there."""
+
+    _cdll: Optional[ctypes.CDLL] = None
+
+    def __getattr__(self, name):
+        if _LazyLibrary._cdll is None:
+            _LazyLibrary._cdll = _load()
+        return getattr(_LazyLibrary._cdll, name)
+
+
+_lib = _LazyLibrary()
+
+
+def load_library() -> ctypes.CDLL:
+    """Map the CUDA library now (ImportError if it is missing or broken) and return it."""
+    _lib.lora_last_error  # noqa: B018  (attribute access maps the library)
+    return _LazyLibrary._cdll
 
 
 def lora_last_error() -> str:

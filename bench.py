@@ -273,8 +273,19 @@ while True:
     el = time.perf_counter() - t0
     if ({fixed_steps} > 0 and steps >= {fixed_steps}) or ({fixed_steps} <= 0 and el >= {seconds}):
         break
-print("RESULT " + json.dumps({{"tokens": tokens, "seconds": el, "steps": steps, "rows_per_step": m}}))
+print("RESULT " + json.dumps({{"tokens": tokens, "seconds": el, "steps": steps, "rows_per_step": m,
+                              "product_library_mapped": bench.product_library_mapped()}}))
 """
+
+
+def product_library_mapped():
+    """Whether this process has the CUDA product library mapped (None where /proc is absent).
+    The CPU-oracle legs must not: they time the oracle alone."""
+    try:
+        with open("/proc/self/maps") as f:
+            return "liblora_gb300" in f.read()
+    except OSError:
+        return None
 
 
 def run_cpu_oracle(workload, layers, tokens, seconds=10.0, fixed_steps=0, warmup=1, step_budget=0.0):
@@ -314,7 +325,8 @@ def reference_arm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": desc,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["cores"], "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "product_library_mapped": {"arm": product_library_mapped(), "oracle_child": d["product_library_mapped"]}}
     print(json.dumps(line), flush=True)
 
 

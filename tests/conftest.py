@@ -21,4 +21,5 @@ def lib():
         pytest.fail("GPU test run without a CUDA device")
     import adapter_gemm_segment_gb300 as ags
 
+    ags.load_library()  # no fallback: a missing library fails every GPU test here
     return ags

@@ -28,3 +28,15 @@ def test_reference_arm_json_line():
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["value"] == d["value"] and cpu["cores"] >= 1 and cpu["sample"]
     assert "workload" in d["config"]
+    # the reference arm times the oracle alone: neither it nor its oracle child maps the CUDA library
+    assert d["product_library_mapped"] == {"arm": False, "oracle_child": False}
+
+
+def test_host_only_package_users_do_not_map_the_library():
+    """Importing the package and its seeded input generators maps no CUDA library (the binding
+    maps it on the first call into it)."""
+    code = ("import adapter_gemm_segment_gb300 as a, adapter_gemm_segment_gb300.workloads as w; "
+            "w.decode_q_proj(seed=1, n=4, layer=0); import bench; print(bench.product_library_mapped())")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert out.stdout.strip().splitlines()[-1] == "False"
