@@ -36,7 +36,7 @@ EXPORTED = (
     "lora_set_timing_events", "lora_linear_fwd_static_ws", "lora_linear_fwd_ex", "lora_pool_load_slots",
     "lora_linear_group_workspace_bytes", "lora_linear_fwd_group", "lora_linear_group_policy",
     "lora_cache_create", "lora_cache_destroy", "lora_cache_register", "lora_cache_unregister", "lora_cache_map",
-    "lora_cache_slot_of", "lora_cache_stats",
+    "lora_cache_slot_of", "lora_cache_stats", "lora_wait_selftest", "lora_set_kernel_stamps",
 )
 
 
@@ -90,6 +90,8 @@ def _load() -> ctypes.CDLL:
         "lora_cache_map": [vp, P(ctypes.c_int64), i32, P(ctypes.c_int32), P(i32), vp],
         "lora_cache_slot_of": [vp, ctypes.c_int64, P(i32)],
         "lora_cache_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64)],
+        "lora_wait_selftest": [vp, vp, i32, i32, ctypes.c_uint64, vp],
+        "lora_set_kernel_stamps": [vp, i32],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -137,6 +139,28 @@ def lora_set_timing_events(before_shrink=None, before_gemm=None, after_gemm=None
         return ctypes.c_void_p(0 if e is None else e.cuda_event)
 
     _check(_lib.lora_set_timing_events(h(before_shrink), h(before_gemm), h(after_gemm)))
+
+
+def lora_set_kernel_stamps(stamps: Optional[torch.Tensor] = None) -> None:
+    """While set (a device int64 tensor [pairs, 2]), every base-GEMM launch records the
+    %globaltimer of its first CTA's start and last CTA's end into the next pair (round robin);
+    initialise pairs to (-1, 0) (unsigned: UINT64_MAX, 0).  No argument disables."""
+    if stamps is None:
+        _check(_lib.lora_set_kernel_stamps(ctypes.c_void_p(0), 0))
+        return
+    if stamps.dtype != torch.int64 or stamps.dim() != 2 or stamps.shape[1] != 2 or not stamps.is_contiguous():
+        raise ValueError("stamps must be a contiguous int64 tensor of shape [pairs, 2]")
+    _check(_lib.lora_set_kernel_stamps(_ptr(_dev(stamps, "stamps")), int(stamps.shape[0])))
+
+
+def lora_wait_selftest(status: torch.Tensor, out: torch.Tensor, arrive: bool, limit_ns: int, stream=None) -> None:
+    """Run the library's bounded pipeline wait on a barrier that completes only if ``arrive``:
+    a wait that gives up sets status (device int32 [1]) to LORA_ETIMEOUT and leaves out
+    (device float32) unwritten; otherwise out is filled with 1.0."""
+    if status.dtype != torch.int32 or out.dtype != torch.float32:
+        raise ValueError("status must be int32 and out float32")
+    _check(_lib.lora_wait_selftest(_ptr(_dev(status, "status")), _ptr(_dev(out, "out")), out.numel(),
+                                   1 if arrive else 0, int(limit_ns), _stream(stream)))
 
 
 def _check(rc: int) -> None:
@@ -261,9 +285,10 @@ def lora_linear_fwd_ex(pool_handle, W: torch.Tensor, x: torch.Tensor, y: torch.T
 
 def lora_linear_fwd_static_ws(pool_handle, W: torch.Tensor, x: torch.Tensor, y: torch.Tensor, seg: lora_segments,
                               variant: int = LORA_VARIANT_AUTO, stream=None) -> torch.Tensor:
-    """lora_linear_fwd for callers that cannot provide a workspace: the library's own fixed
-    4 MiB device array holds the shrink output.  Calls that may overlap on the GPU share it
-    and race; the first call on a device must come before any stream capture."""
+    """lora_linear_fwd for callers that cannot allocate a workspace: the library's own fixed
+    4 MiB device array holds the shrink output (LORA_ENOSPACE beyond it).  The pool's device
+    must be current.  Calls that may overlap on the GPU share the array and race; the first
+    call on a device (which looks the array up) must come before any stream capture."""
     _check(_lib.lora_linear_fwd_static_ws(pool_handle, _ptr(_dev(W, "W")), _ptr(_dev(x, "x")), _ptr(_dev(y, "y")),
                                           ctypes.byref(seg), variant, _stream(stream)))
     return y

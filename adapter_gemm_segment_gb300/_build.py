@@ -61,7 +61,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
                 print(out)
     objs = [j[1] for j in jobs]
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs, "-lcuda" if False else "-lrt"]
+        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs, "-lrt"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")

@@ -28,6 +28,17 @@ int set_error(int code, const char* fmt, ...) {
 
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+static unsigned long long* g_stamps = nullptr;
+static int g_stamp_pairs = 0;
+static int g_stamp_next = 0;
+
+unsigned long long* take_kernel_stamp() {
+    if (!g_stamps || g_stamp_pairs <= 0) return nullptr;
+    unsigned long long* p = g_stamps + 2 * (size_t)g_stamp_next;
+    g_stamp_next = (g_stamp_next + 1) % g_stamp_pairs;
+    return p;
+}
+
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -97,6 +108,15 @@ extern "C" {
 const char* lora_last_error(void) { return g_err; }
 
 uint64_t lora_kernel_launch_count(void) { return g_launches.load(); }
+
+int lora_set_kernel_stamps(void* stamps_dev, int pairs) {
+    if (stamps_dev && pairs <= 0) return set_error(LORA_EINVAL, "pairs must be > 0");
+    if (reinterpret_cast<uintptr_t>(stamps_dev) % 8) return set_error(LORA_EINVAL, "stamps must be 8-byte aligned");
+    g_stamps = static_cast<unsigned long long*>(stamps_dev);
+    g_stamp_pairs = stamps_dev ? pairs : 0;
+    g_stamp_next = 0;
+    return LORA_OK;
+}
 
 int lora_set_timing_events(void* before_shrink, void* before_gemm, void* after_gemm) {
     g_ev_before_shrink = static_cast<cudaEvent_t>(before_shrink);

@@ -21,6 +21,7 @@ struct lora_pool {
     void* B;
     std::vector<uint8_t> mounted;  // host mirror of the slot states this handle enqueued
     std::vector<int> ranks;        // true rank of each mounted slot (host mirror)
+    int device = -1;               // CUDA device that holds the pool's memory
     bool top_dirty = true;         // top_chunks needs recomputing
     int top_chunks[33] = {};       // see PoolView::top_chunks
 };
@@ -160,6 +161,22 @@ void count_launch(int n = 1);
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args);
 
 // ---- device helpers -----------------------------------------------------------------------
+
+// Benchmark instrumentation (off unless lora_set_kernel_stamps is set): a launch records the
+// %globaltimer of its first CTA's start and of its last CTA's end into a pair the host handed
+// out.  Two atomics per CTA, no serialisation of neighbouring launches.
+unsigned long long* take_kernel_stamp();
+__device__ __forceinline__ unsigned long long stamp_clock() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void stamp_start(unsigned long long* st) {
+    if (st != nullptr && threadIdx.x == 0) atomicMin(st, stamp_clock());
+}
+__device__ __forceinline__ void stamp_end(unsigned long long* st) {
+    if (st != nullptr && threadIdx.x == 0) atomicMax(st + 1, stamp_clock());
+}
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

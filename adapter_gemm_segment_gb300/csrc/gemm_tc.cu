@@ -13,9 +13,11 @@
 //
 // Decode (n <= 256 tokens): swap-AB.  The weight tile (128 output features) is the MMA M side
 // and the tokens (padded to a multiple of 16) the N side, so the whole batch is one N tile and
-// W streams through exactly once.  K is split over CTAs to fill the GPU; partial sums go to a
-// float32 workspace and the last CTA of each tile (arrival counter) reduces them in split
-// order, adds the LoRA term and stores y.
+// W streams through exactly once.  K is split over the CTAs of a thread-block cluster (up to 8)
+// to fill the GPU: each CTA parks its float32 partial tile in shared memory, the partials are
+// exchanged by shared-to-remote-shared bulk copies (DSMEM) so that each CTA of the cluster owns
+// a slice of the tokens, and each CTA sums its slice in split order, adds the LoRA term and
+// stores its tokens of y with a TMA store.
 //
 // Prefill (n > 256): 128-token x 256-feature tiles, persistent CTAs over the tile list,
 // double-buffered accumulators (2 x 256 TMEM columns) so the epilogue of one tile overlaps the
@@ -61,6 +63,7 @@ struct DecodeArgs {
     int push;     // exchange partials by bulk copies (1) or remote loads (0)
     const char* prefetch;  // optional range streamed into L2 once this CTA's accumulator is complete
     size_t prefetch_bytes;
+    unsigned long long* stamp;  // benchmark instrumentation (nullptr: off)
 };
 
 struct PrefillArgs {
@@ -70,6 +73,7 @@ struct PrefillArgs {
     const float* s_in;
     void* y;
     int n, m_tiles, n_tiles, kb_total, stages, fuse, bf16;
+    unsigned long long* stamp;  // benchmark instrumentation (nullptr: off)
 };
 
 // Tile order of the persistent prefill kernel: output columns in groups of kPrefillNGroup
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmYtail,
                    const __grid_constant__ CUtensorMap tmB, const DecodeArgs a) {
+    stamp_start(a.stamp);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
@@ -709,6 +714,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     tc_fence_before();
     cluster_sync();  // no CTA leaves while its parked rows may still be copied or read
     if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+    stamp_end(a.stamp);
 }
 
 // ============================================================================================
@@ -719,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const PrefillArgs a) {
     constexpr int BN = kPrefillBN;
+    stamp_start(a.stamp);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
@@ -921,6 +928,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, 2 * BN);
+    stamp_end(a.stamp);
 }
 
 // ============================================================================================
@@ -936,12 +944,14 @@ struct TallArgs {
     void* y;
     int n, n_pad, ldy, h_out, nkb, stages, bf16;
     int tstep;  // tokens per CTA (grid.y splits the batch when the row tiles fill few SMs)
+    unsigned long long* stamp;  // benchmark instrumentation (nullptr: off)
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tall_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const TallArgs a) {
+    stamp_start(a.stamp);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align(smem_raw, 1024);
     const int stages = a.stages;
@@ -1053,6 +1063,7 @@ gemm_tall_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, cols);
+    stamp_end(a.stamp);
 }
 
 // ============================================================================================
@@ -1215,6 +1226,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.push = p.push;
         a.prefetch = static_cast<const char*>(prefetch);
         a.prefetch_bytes = prefetch ? prefetch_bytes : 0;
+        a.stamp = take_kernel_stamp();
         static bool attr_set = false;
         if (!attr_set) {
             LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1263,6 +1275,7 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     a.stages = std::min(4, kSmemBudget / stage_bytes);
     a.fuse = fuse ? 1 : 0;
     a.bf16 = bf16;
+    a.stamp = take_kernel_stamp();
     CUtensorMap mX, mW;
     int rc = make_map(&mX, x, bf16, pv.h_in, n, BM);
     if (rc) return rc;
@@ -1303,6 +1316,7 @@ static int launch_tall_t(const PoolView& pv, const SegView& sv, const void* W, c
     a.h_out = pv.h_out;
     a.nkb = (pv.h_in + BK - 1) / BK;
     a.bf16 = pv.dtype == LORA_BF16;
+    a.stamp = take_kernel_stamp();
     const size_t stage_bytes = (size_t)2 * BM * BK * 2 + (size_t)a.n_pad * BK * 2;
     a.stages = std::max(2, std::min(6, (int)(kSmemBudget / stage_bytes)));
     const size_t smem = (size_t)a.stages * stage_bytes + (2 * (size_t)a.stages + 1) * 8 + 16 + 1024;

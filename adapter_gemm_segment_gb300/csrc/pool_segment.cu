@@ -382,6 +382,12 @@ int lora_pool_create(const lora_pool_desc* desc, void* dev_mem, size_t bytes, vo
     p->B = p->base + L.B_off;
     p->mounted.assign(desc->n_slots, 0);
     p->ranks.assign(desc->n_slots, 0);
+    cudaPointerAttributes attr;  // the device that holds dev_mem (else the current device)
+    if (cudaPointerGetAttributes(&attr, dev_mem) == cudaSuccess &&
+        (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged))
+        p->device = attr.device;
+    else if (cudaGetDevice(&p->device) != cudaSuccess)
+        p->device = -1;
     *out = p;
     return LORA_OK;
 }

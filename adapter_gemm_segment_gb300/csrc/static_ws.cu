@@ -2,21 +2,26 @@
 // a workspace.
 //
 // Some hosts cannot allocate device memory when they call into this library.  One example is
-// a plugin or operator that runs inside someone else's engine, which hands it only its
-// inputs and outputs.  Another is code that enqueues work while a CUDA graph is being
-// captured, or under a fixed memory budget that does not allow growth.  In those settings
-// cudaMalloc is not an option: it synchronises the device, it is not allowed during stream
-// capture, and it may be forbidden by the host.
+// an operator plugin that runs inside someone else's engine: the engine hands it its inputs
+// and outputs and owns every allocation, so the plugin has no allocator of its own.  Another
+// is a host that runs under a fixed device-memory budget set at start-up and may not grow it.
+// For them cudaMalloc is not an option (besides, it synchronises the device).
 //
 // For them, the shrink output that lora_linear_fwd keeps in the caller's workspace lives here
-// in a fixed device array that belongs to the library.  Every GPU that loads the library
-// holds kStaticWsBytes of it until the process exits.
+// in a fixed device array that belongs to the library (g_static_ws, kStaticWsBytes).  Every GPU
+// that loads the library holds it until the process exits.  Batches that need more are refused
+// with LORA_ENOSPACE.
 //
-// The first call on a device looks up the array's device address with
-// cudaGetSymbolAddress and caches it; make that first call before any stream capture.  All
-// calls share the one array: calls that may run at the same time on the GPU (different
-// streams, or graphs replayed concurrently) overwrite each other's data.  Nothing in the
-// array has to start at zero -- every value a call reads was written earlier in the same call.
+// In host code g_static_ws names a host-side stand-in, not the device array, so the kernels get
+// its device address: the first call on a device looks it up with cudaGetSymbolAddress while
+// that device is current, checks the result, and caches it per device.  Make that first call
+// before any stream capture.  The pool's device must be the current device.
+//
+// All calls share the one array, which keeps whatever the last call wrote: calls that may run
+// at the same time on the GPU (different streams, or graphs replayed concurrently) overwrite
+// each other's data.  Nothing in it has to start at zero -- every value a call reads was
+// written earlier in the same call (the shrink writes every element of s that the GEMM or the
+// expand reads).
 #include <mutex>
 
 #include "common.cuh"
@@ -33,11 +38,15 @@ __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 std::mutex g_static_ws_mu;
 void* g_static_ws_ptr[kMaxDevices] = {};
 
-// Device address of g_static_ws on the current device (looked up once per device).
-int static_ws_address(void** out) {
+// Device address of g_static_ws on the pool's device, which must be the current device
+// (looked up once per device, with that device current).
+int static_ws_address(int pool_device, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_error(LORA_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (pool_device >= 0 && dev != pool_device)
+        return set_error(LORA_EINVAL, "the pool lives on device %d but device %d is current: make the pool's device "
+                                      "current before the call", pool_device, dev);
     if (dev < 0 || dev >= kMaxDevices) return set_error(LORA_EUNSUP, "device ordinal %d >= %d", dev, kMaxDevices);
     std::lock_guard<std::mutex> lock(g_static_ws_mu);
     if (!g_static_ws_ptr[dev]) {
@@ -78,7 +87,7 @@ extern "C" int lora_linear_fwd_static_ws(lora_pool_t pool, const void* W_dev, co
                          "with a caller workspace",
                          kStaticWsBytes, need, n, pv.R);
     void* ws = nullptr;
-    int rc = static_ws_address(&ws);
+    int rc = static_ws_address(pool->device, &ws);
     if (rc) return rc;
     float* s_buf = static_cast<float*>(ws);
     if (variant == LORA_VARIANT_AUTO) lora_linear_policy(pool, n, &variant);

@@ -201,17 +201,22 @@ int lora_linear_fwd_ex(lora_pool_t pool, const void* W_dev, const void* x_dev, v
                        const lora_segments* seg, int variant, void* ws_dev, size_t ws_bytes,
                        const void* prefetch_dev, size_t prefetch_bytes, void* stream);
 
-/* lora_linear_fwd without a caller workspace (the multi-LoRA pages have no counterpart; this
- * is a convenience of this library).  For hosts that cannot allocate device memory when they
- * call in -- for example a plugin inside another engine that is handed only its inputs and
- * outputs, or code enqueueing during CUDA graph capture, where cudaMalloc is not allowed.
+/* lora_linear_fwd without a caller workspace.  The multi-LoRA pages have no counterpart to
+ * this entry point: it is a convenience of this library for callers that cannot allocate
+ * device memory when they call in -- for example an operator plugin inside another engine,
+ * which is handed only its inputs and outputs while the engine owns every allocation, or a
+ * host held to a fixed device-memory budget that it may not grow.
  * Arguments and results are those of lora_linear_fwd; the shrink output goes to a fixed
- * 4 MiB device array owned by the library (held on every GPU that loads the library until the
- * process exits), so calls that need more (4 * n * r_max * ceil(h_in/1024) bytes for batches
- * of up to 256 tokens, 4 * n * r_max above) fail with LORA_ENOSPACE.  This function allocates
- * nothing.  Its first call on a device looks up the array's address (cudaGetSymbolAddress);
- * make that first call before any stream capture.  All calls share the array, so calls that
- * can overlap on the GPU (several streams, concurrent graph replays) race with each other. */
+ * 4 MiB device array owned by the library (a static device array: every GPU that loads the
+ * library holds it until the process exits).  A call needs 4 * n * r_max * p bytes of it, with
+ * p = min(ceil(h_in / 1024), 4, max(1, 256 / n)) for 16-bit batches of up to 256 tokens and
+ * p = 1 otherwise; larger calls fail with LORA_ENOSPACE and enqueue nothing.  This function
+ * calls no cudaMalloc, cudaFree or allocating library routine.  The pool's device must be the
+ * current device (LORA_EINVAL otherwise).  Its first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  Every call shares the array, which keeps the last call's contents (a
+ * call reads only values it wrote itself, so nothing has to start at zero); calls that can
+ * overlap on the GPU (several streams, concurrent graph replays) race with each other. */
 int lora_linear_fwd_static_ws(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev,
                               const lora_segments* seg, int variant, void* stream);
 
@@ -296,6 +301,16 @@ int lora_cache_map(lora_cache_t cache, const int64_t* ids, int n, int32_t* idx_o
 int lora_cache_slot_of(lora_cache_t cache, int64_t id, int* slot);
 int lora_cache_stats(lora_cache_t cache, uint64_t* hits, uint64_t* misses, uint64_t* evictions);
 
+/* Diagnostic of the failure path (the pages have no counterpart).  Every pipeline wait of
+ * the tensor-core kernels is bounded: when one runs past its limit the kernel records
+ * LORA_ETIMEOUT in the status word, writes none of its output and returns (no trap, no
+ * endless spin).  This call runs that same bounded wait in one small kernel on `stream`:
+ * the kernel waits on a barrier that completes only if `arrive` is non-zero, for at most
+ * limit_ns nanoseconds (<= 100 ms, LORA_EINVAL above).  If the wait gives up, *status_dev
+ * (device int32) becomes LORA_ETIMEOUT and out_dev is not written; otherwise out_dev[0..n)
+ * (device float32, n <= 2^20) is set to 1.0 and *status_dev is left as it was. */
+int lora_wait_selftest(int32_t* status_dev, float* out_dev, int n, int arrive, uint64_t limit_ns, void* stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* lora_last_error(void);
 
@@ -308,6 +323,17 @@ uint64_t lora_kernel_launch_count(void);
  * base-GEMM kernel.  The records serialise those kernels (no launch overlap), so the
  * intervals are per-kernel durations.  Process-wide, not thread-safe; NULLs disable. */
 int lora_set_timing_events(void* before_shrink, void* before_gemm, void* after_gemm);
+
+/* In-step timing instrumentation for benchmarks: while set, every base-GEMM launch (decode,
+ * prefill and tall-tile kernels) takes the next of `pairs` pairs of uint64 in stamps_dev
+ * (device memory, 8-byte aligned; round robin in launch order, restarting at pair 0 on every
+ * call of this function) and records into it the %globaltimer nanoseconds of its first CTA's
+ * start (atomicMin into [0]) and of its last CTA's end (atomicMax into [1]); the caller sets
+ * every pair to {UINT64_MAX, 0} before the launches it times.  Unlike lora_set_timing_events
+ * this does not serialise neighbouring launches, so the intervals are the kernels' durations
+ * inside a chain of programmatic dependent launches.  Process-wide, not thread-safe; NULL
+ * disables.  LORA_EINVAL for pairs <= 0 with a buffer, or a misaligned buffer. */
+int lora_set_kernel_stamps(void* stamps_dev, int pairs);
 
 #ifdef __cplusplus
 }

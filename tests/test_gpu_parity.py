@@ -32,13 +32,49 @@ def make_pool(ags, case, n_slots=None, load=True):
     return pool
 
 
+class Guarded:
+    """A device buffer between two guard zones of canary bytes (the stand-in for a memory
+    checker): a kernel writing past either end of the buffer it was given changes a canary.
+    The interior starts as canary bytes too (or NaN for outputs), so results cannot depend
+    on the library finding zeros in its workspaces."""
+
+    ZONE = 4096
+    CANARY = 0xA5
+
+    def __init__(self, nbytes, what):
+        self.nbytes, self.what = int(nbytes), what
+        pad = (self.nbytes + 255) // 256 * 256
+        self.full = torch.full((2 * self.ZONE + pad,), self.CANARY, dtype=torch.uint8, device=DEV)
+        self.bytes = self.full[self.ZONE:self.ZONE + self.nbytes]
+
+    @classmethod
+    def tensor(cls, shape, dtype, what):
+        es = torch.empty(0, dtype=dtype).element_size()
+        g = cls(int(np.prod(shape)) * es, what)
+        g.t = g.bytes.view(dtype).view(*shape)
+        g.t.fill_(float("nan"))
+        return g
+
+    def check(self):
+        z = self.ZONE
+        front, back = self.full[:z], self.full[z + self.nbytes:]
+        assert bool((front == self.CANARY).all()), f"{self.what}: write before the start of the buffer"
+        assert bool((back == self.CANARY).all()), f"{self.what}: write past the end of the buffer"
+
+
 def run(ags, case, variant=0, W=None, idx=None, pool=None):
     pool = pool or make_pool(ags, case)
     idx = case.idx if idx is None else idx
-    seg = pool.segment(idx.to(DEV))
+    n = int(idx.numel())
+    seg_g = Guarded(ags.lora_segment_workspace_bytes(n, pool.n_slots), "segment workspace")
+    seg = pool.segment(idx.to(DEV), ws=seg_g.bytes)
+    lin_g = Guarded(ags.lora_linear_workspace_bytes(pool.handle, n), "linear workspace")
+    y_g = Guarded.tensor((n, case.h_out), case.dtype, "y")
     Wd = (case.W if W is None else W).to(DEV)
-    y = pool.linear(Wd, case.x.to(DEV), seg, variant=variant)
+    y = pool.linear(Wd, case.x.to(DEV), seg, variant=variant, y=y_g.t, ws=lin_g.bytes)
     torch.cuda.synchronize()
+    for g in (seg_g, lin_g, y_g):
+        g.check()
     return y.cpu(), pool, seg
 
 
@@ -365,6 +401,71 @@ def test_full_layer_sampled(lib):
 
 
 # ------------------------------------------------------------------------------------------
+# the full-size configurations through the exact calls the benchmark times
+# ------------------------------------------------------------------------------------------
+
+LAYER_GROUPS = (("q_proj", "k_proj", "v_proj"), ("o_proj",), ("gate_proj", "up_proj"), ("down_proj",))
+
+
+def _negative_control(y0, cases, pools_ref, rows=None, seed=5):
+    """The LoRA-only output against the oracle of a shuffled routing must fail somewhere."""
+    idx = cases[0].idx.numpy()
+    shuffled = np.random.default_rng(seed).permutation(idx)
+    if np.array_equal(shuffled, idx):
+        return
+    wrong = O.lora_linear_group(cases[0].x, [torch.zeros_like(c.W) for c in cases], pools_ref, shuffled, rows=rows)
+    assert not O.within_tolerance(y0, wrong).all(), "a shuffled routing passes the LoRA-only check"
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_full_layer_grouped_every_row(lib, variant):
+    """The 7B-shaped layer (256 tokens bf16, rank 16, 100 adapters, Zipf) as the benchmark runs
+    it: q|k|v, o, gate|up and down as four grouped calls (the 256-row-tile GEMM with its token
+    split for q|k|v and gate|up under the policy).  Every row of every call against the oracle,
+    a LoRA-only run (W = 0) of each, and a negative control."""
+    cases = {c.name.split("_", 1)[1]: c for c in wl.full_layer(layer=0)}
+    for names in LAYER_GROUPS:
+        group = [cases[nm] for nm in names]
+        pools_ref = [O.pool_of_case(c) for c in group]
+        y, pools, _ = run_group(lib, group, variant)
+        ref = O.lora_linear_group(group[0].x, [c.W for c in group], pools_ref, group[0].idx.numpy())
+        assert_parity(y, ref, f"{'|'.join(names)} variant {variant}")
+        y0, _, _ = run_group(lib, group, variant, pools=pools, zero_w=True)
+        ref0 = O.lora_linear_group(group[0].x, [torch.zeros_like(c.W) for c in group], pools_ref,
+                                   group[0].idx.numpy())
+        assert_lora_only_parity(y0, ref0, f"{'|'.join(names)} W=0 variant {variant}")
+        _negative_control(y0, group, pools_ref)
+        del pools
+
+
+def _prefill_rows():
+    """One whole 128-token tile of every 512-token request (a different tile position per
+    request), the first and last token of every request, and a seeded sample."""
+    rows = [np.arange(512 * i + 128 * (i % 4), 512 * i + 128 * (i % 4) + 128) for i in range(32)]
+    rows.append(np.concatenate([[512 * i, 512 * i + 511] for i in range(32)]))
+    rows.append(np.random.default_rng(8).choice(16384, 256, replace=False))
+    return np.unique(np.concatenate(rows))
+
+
+@pytest.mark.parametrize("variant", [0, 2])
+def test_prefill_grouped_tiles(lib, variant):
+    """Prefill (32 x 512 tokens bf16) as the benchmark runs it: q_proj and v_proj as one grouped
+    call (the grouped tensor-core shrink and the 8192-wide prefill GEMM under the policy)."""
+    group = wl.prefill()
+    rows = _prefill_rows()
+    pools_ref = [O.pool_of_case(c) for c in group]
+    y, pools, seg = run_group(lib, group, variant)
+    check_segments(lib, seg, group[0].idx.numpy(), 100, group[0].adapters.ranks)
+    ref = O.lora_linear_group(group[0].x, [c.W for c in group], pools_ref, group[0].idx.numpy(), rows=rows)
+    assert_parity(y[rows], ref, f"prefill q|v variant {variant}")
+    y0, _, _ = run_group(lib, group, variant, pools=pools, zero_w=True)
+    ref0 = O.lora_linear_group(group[0].x, [torch.zeros_like(c.W) for c in group], pools_ref,
+                               group[0].idx.numpy(), rows=rows)
+    assert_lora_only_parity(y0[rows], ref0, f"prefill q|v W=0 variant {variant}")
+    _negative_control(y0[rows], group, pools_ref, rows=rows)
+
+
+# ------------------------------------------------------------------------------------------
 # segments shared by pools whose slots hold different ranks
 # ------------------------------------------------------------------------------------------
 
@@ -396,18 +497,24 @@ def group_pools(ags, cases):
 def run_group(ags, cases, variant=0, pools=None, zero_w=False, ws=None):
     pools = pools or group_pools(ags, cases)
     x, idx = cases[0].x.to(DEV), cases[0].idx.to(DEV)
-    seg = pools[0].segment(idx)
+    n = cases[0].n
+    seg_g = Guarded(ags.lora_segment_workspace_bytes(n, pools[0].n_slots), "segment workspace")
+    seg = pools[0].segment(idx, ws=seg_g.bytes)
     W = torch.cat([c.W for c in cases], 0).to(DEV)
     if zero_w:
         W.zero_()
-    n = cases[0].n
-    y = torch.full((n, W.shape[0]), float("nan"), dtype=cases[0].dtype, device=DEV)
+    y_g = Guarded.tensor((n, W.shape[0]), cases[0].dtype, "y")
     handles = [p.handle for p in pools]
+    guards = [seg_g, y_g]
     if ws is None:
-        ws = ags._device_bytes(ags.lora_linear_group_workspace_bytes(handles, n), DEV)
-    ags.lora_linear_fwd_group(handles, W, x, y, seg, ws, variant)
+        ws_g = Guarded(ags.lora_linear_group_workspace_bytes(handles, n), "group workspace")
+        ws = ws_g.bytes
+        guards.append(ws_g)
+    ags.lora_linear_fwd_group(handles, W, x, y_g.t, seg, ws, variant)
     torch.cuda.synchronize()
-    return y.cpu(), pools, seg
+    for g in guards:
+        g.check()
+    return y_g.t.cpu(), pools, seg
 
 
 def group_ref(cases, zero_w=False):

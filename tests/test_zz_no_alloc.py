@@ -1,15 +1,16 @@
 """The workspace-free linear forward (lora_linear_fwd_static_ws).
 
-It serves callers that cannot hand the library any device memory of their own -- a plugin
-inside another engine that only receives its inputs and outputs, or code enqueueing work
-during CUDA graph capture, where cudaMalloc is not allowed.  Its scratch is a fixed device
-array inside the library.  This file runs last (pytest collects files in name order), so a
-run that stops at the first failure has executed every other test before it.
+It serves callers that cannot hand the library any device memory of their own -- an operator
+plugin inside another engine that only receives its inputs and outputs while the engine owns
+every allocation, or a host held to a fixed device-memory budget.  Its scratch (the shrink
+output) is a fixed device array inside the library.  This file runs last (pytest collects
+files in name order), so a run that stops at the first failure has executed every other test
+before it; it also passes when run alone in a fresh process.
 
-Each case is called twice in a row through the C ABI, and both results must agree with the
-regular entry point (caller workspace) within the same tolerance the parity tests use.
+Each case is called twice in a row through the C ABI.  Both results must equal the regular
+entry point's (caller workspace) bit for bit: the kernels and their inputs are the same, only
+the address of the scratch differs.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -19,15 +20,13 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     ("decode fp16 n=64", lambda: wl.random_case(31, 64, 1024, 512, [8, 8, 8, 8], r_max=8, dtype=torch.float16)),
+    # h_in 4096 at 64 tokens: the decode shrink writes 4 K-parts (64 x 8 x 4 floats of scratch)
+    ("decode fp16 n=64 h_in=4096, 4 shrink parts",
+     lambda: wl.random_case(34, 64, 4096, 256, [8, 8, 8], r_max=8, dtype=torch.float16)),
     ("mixed rank n=7", lambda: wl.random_case(32, 7, 512, 256, [8, 16, 64], r_max=64, dtype=torch.float16)),
     ("long batch bf16 n=300", lambda: wl.random_case(33, 300, 512, 384, [16, 16], r_max=16, dtype=torch.bfloat16)),
     ("fp32 n=16", lambda: wl.tiny()),
 ]
-
-
-def _close(a: torch.Tensor, b: torch.Tensor) -> bool:
-    a64, b64 = a.double().cpu().numpy(), b.double().cpu().numpy()
-    return bool(np.all(np.abs(a64 - b64) <= 1e-2 + 1e-2 * np.abs(b64)))
 
 
 @pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
@@ -46,8 +45,8 @@ def test_static_workspace_matches_caller_workspace(lib, name, make):
         lib.lora_linear_fwd_static_ws(pool.handle, W, x, y, seg)
         outs.append(y)
     torch.cuda.synchronize()
-    for y in outs:
-        assert _close(y, y_ref), f"{name}: static-workspace result differs from the caller-workspace result"
+    for k, y in enumerate(outs):
+        assert torch.equal(y, y_ref), f"{name}: call {k + 1} differs from the caller-workspace result"
 
 
 def test_static_workspace_refuses_oversized_batches(lib):
