@@ -37,6 +37,8 @@ EXPORTED = (
     "lora_linear_group_workspace_bytes", "lora_linear_fwd_group", "lora_linear_group_policy",
     "lora_cache_create", "lora_cache_destroy", "lora_cache_register", "lora_cache_unregister", "lora_cache_map",
     "lora_cache_slot_of", "lora_cache_stats", "lora_wait_selftest", "lora_set_kernel_stamps",
+    "lora_loader_create", "lora_loader_destroy", "lora_loader_mount", "lora_loader_acquire", "lora_loader_release",
+    "lora_loader_stats",
 )
 
 
@@ -92,6 +94,12 @@ def _load() -> ctypes.CDLL:
         "lora_cache_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64)],
         "lora_wait_selftest": [vp, vp, i32, i32, ctypes.c_uint64, vp],
         "lora_set_kernel_stamps": [vp, i32],
+        "lora_loader_create": [i32, P(vp), vp, P(vp)],
+        "lora_loader_destroy": [vp],
+        "lora_loader_mount": [vp, i32, P(i32), P(vp), P(vp), P(i32), P(ctypes.c_float)],
+        "lora_loader_acquire": [vp, i32, P(i32), vp],
+        "lora_loader_release": [vp, i32, P(i32), vp],
+        "lora_loader_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -421,6 +429,92 @@ class LoraCache:
     def close(self) -> None:
         if self.handle is not None:
             lora_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _slot_array(slots):
+    slots = [int(s) for s in slots]
+    return len(slots), (ctypes.c_int * max(1, len(slots)))(*slots)
+
+
+def lora_loader_create(pool_handles, copy_stream) -> ctypes.c_void_p:
+    count, arr = _handles(pool_handles)
+    h = ctypes.c_void_p()
+    _check(_lib.lora_loader_create(count, arr, _stream(copy_stream), ctypes.byref(h)))
+    return h
+
+
+def lora_loader_destroy(handle) -> None:
+    _check(_lib.lora_loader_destroy(handle))
+
+
+def lora_loader_mount(handle, slots, As, Bs, alphas) -> None:
+    """As[p][i], Bs[p][i]: pinned host tensors of slot slots[i]'s adapter for pool p; alphas[i]
+    its alpha (the same for every pool).  The caller keeps the tensors alive until the copy
+    stream has passed the mount."""
+    count, sl = _slot_array(slots)
+    npools = len(As)
+    flatA = [a for per_pool in As for a in per_pool]
+    flatB = [b for per_pool in Bs for b in per_pool]
+    for t in flatA + flatB:
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("loader mounts read contiguous pinned host memory")
+    Ap = (ctypes.c_void_p * max(1, len(flatA)))(*[a.data_ptr() for a in flatA])
+    Bp = (ctypes.c_void_p * max(1, len(flatB)))(*[b.data_ptr() for b in flatB])
+    ranks = (ctypes.c_int * max(1, len(flatA)))(*[int(a.shape[0]) for a in flatA])
+    al = (ctypes.c_float * max(1, npools * count))(*[float(alphas[i]) for _ in range(npools) for i in range(count)])
+    _check(_lib.lora_loader_mount(handle, count, sl, Ap, Bp, ranks, al))
+
+
+def lora_loader_acquire(handle, slots, stream=None) -> None:
+    count, sl = _slot_array(slots)
+    _check(_lib.lora_loader_acquire(handle, count, sl, _stream(stream)))
+
+
+def lora_loader_release(handle, slots, stream=None) -> None:
+    count, sl = _slot_array(slots)
+    _check(_lib.lora_loader_release(handle, count, sl, _stream(stream)))
+
+
+def lora_loader_stats(handle) -> dict:
+    m, d = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(_lib.lora_loader_stats(handle, ctypes.byref(m), ctypes.byref(d)))
+    return {"mounts": m.value, "drained_fences": d.value}
+
+
+class LoraLoader:
+    """Background mounts into ``LoraPool`` objects (same slot count) on a copy stream, with
+    acquire/release fences for the compute streams (see include/lora.h)."""
+
+    def __init__(self, pools, copy_stream):
+        self.pools = list(pools)
+        self.copy_stream = copy_stream
+        self.handle = lora_loader_create([p.handle for p in self.pools], copy_stream)
+        self._keep = {}
+
+    def mount(self, slots, As, Bs, alphas) -> None:
+        lora_loader_mount(self.handle, slots, As, Bs, alphas)
+        for t in [a for per_pool in As for a in per_pool] + [b for per_pool in Bs for b in per_pool]:
+            self._keep[t.data_ptr()] = t  # host sources stay alive while the copy stream may read them
+
+    def acquire(self, slots, stream=None) -> None:
+        lora_loader_acquire(self.handle, slots, stream)
+
+    def release(self, slots, stream=None) -> None:
+        lora_loader_release(self.handle, slots, stream)
+
+    def stats(self) -> dict:
+        return lora_loader_stats(self.handle)
+
+    def close(self) -> None:
+        if self.handle is not None:
+            lora_loader_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

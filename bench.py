@@ -9,19 +9,29 @@ Workloads (synthetic, seeded, shaped like the multi-LoRA serving pages' 7B model
                      32 layers, each layer with its own base weight, its own pool of 100
                      rank-8/alpha-16 adapters and its own input; idx Zipf(1.1) over 100 slots
                      with 10 % base-only, routed once per batch (one segment build per step).
+                     The line also carries a "prefill" leg (the workload below, measured the
+                     same way), so one run reports both halves of the metric: decode against
+                     the HBM roofline, prefill against the tensor roofline.
   prefill            32 requests x 512 tokens (16384, bf16) through q_proj and v_proj
-                     (4096 x 4096 each, 100 rank-16/alpha-32 adapters per projection).
+                     (4096 x 4096 each, 100 rank-16/alpha-32 adapters per projection), as one
+                     grouped call.
   mixed              one batch of --tokens tokens (1..64) through 32 layer copies of a
                      4096 x 4096 fp16 linear whose 6 adapters have ranks {8,8,16,16,64,64}
                      padded to 64.
+  layer              256 tokens through the 7 projections of 4 7B-shaped layers (grouped
+                     calls q|k|v, o, gate|up, down).
   load               mounts one 7B-shaped rank-8 adapter (224 slots) from pinned host memory
                      (lora_pool_load_slot reads it over NVLink-C2C); ms per adapter.
+  concat             the segmented path against the pages' concatenated-adapter matmul
+                     (cuBLAS baseline) at 1, 8 and 64 tokens.
 A step = one lora_segment + every lora_linear_fwd of the step, captured once in a CUDA graph
 and replayed.  Each step's inputs exceed the 129 MB L2 (no flush needed).
 
-Extra legs: per-kernel CUDA-event timing (roofline of the base-GEMM kernel), end-to-end
-timing with pinned host buffers and host<->device copies inside the timed region, the CPU
-oracle timed on the host cores (cpu_baseline), and SM clocks sampled during the timed region.
+Extra legs: the dominant kernel's time inside the step (%globaltimer stamps of every base-GEMM
+launch in the chained graph; the serialised CUDA-event figure beside it), end-to-end timing
+with pinned host buffers and host<->device copies inside the timed region, the CPU oracle
+timed on the host cores (cpu_baseline), SM clocks sampled during the timed region, and the
+tensor-concatenation figures of the batch (concat_metrics).
 `--impl reference` times the CPU oracle alone (the reference arm of this build).
 """
 from __future__ import annotations
@@ -41,7 +51,7 @@ if ROOT not in sys.path:
 
 METRIC = "LoRA-linear tokens/s at 1 GB300 + % of HBM (decode) / tensor (prefill) roofline"
 UNIT = "tokens/s"
-DEFAULT_STEPS = {"decode": 4000, "mixed": 4000, "prefill": 400, "layer": 1000, "load": 20}
+DEFAULT_STEPS = {"decode": 4000, "mixed": 4000, "prefill": 400, "layer": 1000, "load": 20, "concat": 200}
 
 
 def parse_args():
@@ -50,7 +60,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=None)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["decode", "prefill", "mixed", "layer", "load"], default="decode")
+    p.add_argument("--workload", choices=["decode", "prefill", "mixed", "layer", "load", "concat"], default="decode")
     p.add_argument("--variant", type=int, default=0, help="0 auto, 1 fused, 2 separate, 3 CUDA-core")
     p.add_argument("--ungrouped", action="store_true",
                    help="layer and prefill workloads: one call per projection instead of grouping the projections "
@@ -60,6 +70,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the cpu_baseline leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-prefill-leg", action="store_true",
+                   help="decode workload: skip the prefill leg (the tensor-roofline half of the metric)")
     p.add_argument("--prefetch-next", action="store_true",
                    help="pass the next linear's weight as the L2 prefetch hint of lora_linear_fwd_ex")
     a = p.parse_args()
@@ -356,20 +368,39 @@ def read_profile_traffic(kernel_key):
         return None
 
 
-def ours(args):
+def concat_metrics(idx, h_in, h_out, ranks, r_max, n_slots):
+    """The three figures by which the blog.lonae.com page (tensor-concatenation paragraph)
+    describes a concatenated-adapter matmul, for this batch, plus the segment count:
+      - elements of the concatenated matrices (all n_slots adapters' A and B at r_max): the
+        memory peak of that approach;
+      - its batch x seq projection: the [n, n_slots * r_max] intermediate x A_cat^T, the launch
+        dimension of that approach;
+      - the zero-padding share: the part of the LoRA work done at r_max that multiplies padding,
+        weighted by tokens (the invalid-FLOP share of a padded path) and by the touched adapters'
+        stored rows (bytes);
+    and the share of the concatenated approach's LoRA FLOPs that no token needs."""
+    import numpy as np
+
+    idx = np.asarray(idx)
+    lora = idx[idx >= 0]
+    touched = sorted(set(lora.tolist()))
+    n = int(idx.size)
+    useful_padded = 2 * len(lora) * r_max * (h_in + h_out)
+    concat_flops = 2 * n * n_slots * r_max * (h_in + h_out)
+    tok_pad = float(sum(r_max - ranks[s] for s in lora.tolist())) / (len(lora) * r_max) if len(lora) else 0.0
+    slot_pad = float(sum(r_max - ranks[s] for s in touched)) / (len(touched) * r_max) if touched else 0.0
+    nseg = len(touched) + (1 if (idx < 0).any() else 0)
+    return {"n_segments": nseg, "distinct_adapters": len(touched),
+            "concat_elements": n_slots * r_max * (h_in + h_out), "concat_projection": [n, n_slots * r_max],
+            "concat_projection_elements": n * n_slots * r_max,
+            "zero_pad_flop_share": tok_pad, "zero_pad_stored_share": slot_pad,
+            "concat_lora_flops_wasted_share": (1.0 - useful_padded / concat_flops) if concat_flops else 0.0}
+
+
+def measure(args, wl_name, steps, warmup, world, rank, local, dist, dev, peaks):
+    """Time one workload's step on this rank; returns the JSON object of the line (rank 0)."""
     import numpy as np
     import torch
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=dev)
 
     def barrier():
         if dist is not None:
@@ -377,8 +408,9 @@ def ours(args):
 
     import adapter_gemm_segment_gb300 as ags
 
-    peaks = load_peaks()
-    idx, cases, desc = workload_cases(args.workload, rank, args.layers, args.tokens)
+    tokens = args.tokens if wl_name in ("decode", "mixed") else None
+    n_layers = args.layers if wl_name == args.workload else (4 if wl_name == "layer" else 32)
+    idx, cases, desc = workload_cases(wl_name, rank, n_layers, tokens or 64)
     dtype = cases[0].dtype
     n = int(idx.numel())
     stream = torch.cuda.Stream(dev)
@@ -400,7 +432,7 @@ def ours(args):
                        "y": torch.empty(n, case.h_out, dtype=dtype, device=dev)})
         del A_all, B_all
     # prefill: q and v share x
-    if args.workload == "prefill":
+    if wl_name == "prefill":
         layers[1]["x"] = layers[0]["x"]
     idx_dev = idx.to(dev)
     pool0 = layers[0]["pool"]
@@ -414,7 +446,7 @@ def ours(args):
     # calls of one step: single linears, or (layer workload) groups of projections that read
     # the same x -- q|k|v and gate|up -- as one call over their concatenated weight
     calls = []
-    grouped = args.workload in ("layer", "prefill") and not args.ungrouped
+    grouped = wl_name in ("layer", "prefill") and not args.ungrouped
     i = 0
     while i < len(layers):
         j = i + 1
@@ -435,7 +467,7 @@ def ours(args):
         i = j
     torch.cuda.synchronize()
 
-    prefetch = args.prefetch_next and args.workload != "prefill" and not grouped
+    prefetch = args.prefetch_next and wl_name != "prefill" and not grouped
     nxt = [calls[(i + 1) % len(calls)]["members"][0]["W"] if prefetch else None for i in range(len(calls))]
 
     def linear(i, c, seg):
@@ -472,7 +504,7 @@ def ours(args):
         pass
     clocks = ClockSampler(gpu_id)
     time.sleep(0.3)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()
 
@@ -482,7 +514,7 @@ def ours(args):
     torch.cuda.synchronize()
     t_host0 = time.time()
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         graph.replay()
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -492,9 +524,9 @@ def ours(args):
     time.sleep(0.25)
     clocks.stop()
     clk = clocks.summary(t_host0, t_host1)
-    ms_per_step = ms / args.steps
+    ms_per_step = ms / steps
     tokens_per_step = n * len(layers)
-    value = job_tokens_per_s(world, tokens_per_step, args.steps, ms)
+    value = job_tokens_per_s(world, tokens_per_step, steps, ms)
 
     # ---- per-kernel timing (events recorded around each kernel, graph-replayed) ----
     n_lin = len(calls)
@@ -510,7 +542,7 @@ def ours(args):
             ags.lora_set_timing_events(*trio)
             linear(i, c, seg)
         ags.lora_set_timing_events()
-    reps = max(3, min(50, args.steps // 20))
+    reps = max(3, min(50, steps // 20))
     g2.replay()
     torch.cuda.synchronize()
     t_shr = [[] for _ in range(n_lin)]
@@ -521,9 +553,44 @@ def ours(args):
         for i, trio in enumerate(evs):
             t_shr[i].append(trio[0].elapsed_time(trio[1]))
             t_gemm[i].append(trio[1].elapsed_time(trio[2]))
-    gemm_ms_i = [statistics.mean(v) for v in t_gemm]
+    gemm_ms_ser_i = [statistics.mean(v) for v in t_gemm]
     shrink_ms = statistics.mean(statistics.mean(v) for v in t_shr)
+
+    # ---- in-step kernel time: every base-GEMM launch stamps %globaltimer at its first CTA's
+    # start and its last CTA's end, inside the same chained graph (no events between kernels,
+    # so programmatic dependent launch overlaps exactly as in the timed region) ----
+    stamps = torch.empty(n_lin, 2, dtype=torch.int64, device=dev)
+    ags.lora_set_kernel_stamps(stamps)
+    try:
+        g3 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g3, stream=stream):
+            step()
+    finally:
+        ags.lora_set_kernel_stamps()
+    d_in = [[] for _ in range(n_lin)]
+    step_in = []
+    e3a, e3b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for r in range(reps + 1):
+        stamps[:, 0].fill_(-1)  # UINT64_MAX for the kernels' atomicMin
+        stamps[:, 1].fill_(0)
+        e3a.record(stream)
+        g3.replay()
+        e3b.record(stream)
+        torch.cuda.synchronize()
+        if r == 0:
+            continue
+        st = stamps.cpu()
+        step_in.append(e3a.elapsed_time(e3b))
+        for i in range(n_lin):
+            d_in[i].append(float(st[i, 1] - st[i, 0]) / 1e6 if int(st[i, 0]) > 0 and int(st[i, 1]) > 0 else None)
+    if all(v is not None for d in d_in for v in d):
+        gemm_ms_i = [statistics.mean(v) for v in d_in]
+        timing_basis = "in-step (%globaltimer stamps of every base-GEMM launch inside the chained graph)"
+    else:  # kernels without stamps (CUDA-core diagnostic variant): serialised events only
+        gemm_ms_i = gemm_ms_ser_i
+        timing_basis = "serialised (CUDA events between kernels)"
     gemm_ms = statistics.mean(gemm_ms_i)
+    gemm_ms_ser = statistics.mean(gemm_ms_ser_i)
 
     idx_np = idx.numpy()
     algs = [algorithmic_case(idx_np, c.h_in, c.h_out, c.adapters.r_max) for c in cases]
@@ -531,11 +598,11 @@ def ours(args):
     step_roof_ms = sum(max(a_["linear_bytes"] / (peaks["hbm_gbs"] * 1e9),
                            a_["linear_flops"] / (peaks["bf16_tflops"] * 1e12)) for a_ in algs) * 1e3
     alg = {"D": algs[0]["D"], "n_L": algs[0]["n_L"]}
-    if args.workload == "prefill":
+    if wl_name == "prefill":
         achieved = sum(a_["gemm_flops"] for a_ in algs) / (sum(gemm_ms_i) / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": read_profile_traffic(f"gemm_prefill_{args.workload}"),
+                "traffic": read_profile_traffic(f"gemm_prefill_{wl_name}"),
                 "kernel": "gemm_prefill_kernel", "kernel_ms": gemm_ms,
                 "algorithmic_flops_per_launch": sum(a_["gemm_flops"] for a_ in algs) / n_lin,
                 "peak_source": peaks["source"] + " burst",
@@ -544,11 +611,17 @@ def ours(args):
         achieved = sum(a_["gemm_bytes"] for a_ in algs) / (sum(gemm_ms_i) / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": read_profile_traffic(f"gemm_decode_{args.workload}"),
+                "traffic": read_profile_traffic(f"gemm_decode_{wl_name}"),
                 "kernel": ("base GEMM calls: gemm_tall_kernel (grouped q|k|v, gate|up), gemm_decode_kernel (o, down)"
-                           if args.workload == "layer" and grouped else "gemm_decode_kernel"), "kernel_ms": gemm_ms,
+                           if wl_name == "layer" and grouped else "gemm_decode_kernel"), "kernel_ms": gemm_ms,
                 "algorithmic_bytes_per_launch": sum(a_["gemm_bytes"] for a_ in algs) / n_lin,
                 "peak_source": peaks["source"] + " copy"}
+    alg_per_launch = sum(a_["gemm_flops" if wl_name == "prefill" else "gemm_bytes"] for a_ in algs) / n_lin
+    roof["timing_basis"] = timing_basis
+    roof["kernel_ms_serialised"] = gemm_ms_ser
+    roof["frac_serialised"] = alg_per_launch / (gemm_ms_ser / 1e3) / (peak * (1e12 if wl_name == "prefill" else 1e9))
+    roof["kernels_ms_sum_over_step_ms"] = sum(gemm_ms_i) / statistics.mean(step_in)
+    roof["instrumented_step_ms"] = statistics.mean(step_in)
     roof["shrink_ms"] = shrink_ms
     roof["step_roofline_ms"] = step_roof_ms
     roof["step_frac"] = step_roof_ms / ms_per_step
@@ -594,7 +667,7 @@ def ours(args):
         y_host = [[torch.empty(y.shape, dtype=dtype, pin_memory=True) for y in b["y"]] for b in sets]
         h2d = idx_host.numel() * 4 + sum(v.numel() * v.element_size() for v in x_host.values())
         d2h = sum(y.numel() * y.element_size() for y in y_host[0])
-        e2e_steps = max(3, min(args.steps, 500))
+        e2e_steps = max(3, min(steps, 500))
         h2d_st, d2h_st = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         loaded = [torch.cuda.Event() for _ in range(2)]
         computed = [torch.cuda.Event() for _ in range(2)]
@@ -638,7 +711,7 @@ def ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        d = run_cpu_oracle(args.workload, args.layers, args.tokens, seconds=args.cpu_seconds)
+        d = run_cpu_oracle(wl_name, n_layers, tokens or 64, seconds=args.cpu_seconds)
         cpu = {"value": d["tokens"] / d["seconds"], "unit": UNIT, "cores": d["cores"], "kind": "oracle",
                "sample": f"{d['steps']} passes of one linear of the workload ({d['rows_per_step']} tokens each, "
                          f"float64 numpy oracle) in {d['seconds']:.1f} s"}
@@ -648,17 +721,50 @@ def ours(args):
         cfg.update({"variant": {0: "auto", 1: "fused", 2: "separate", 3: "cuda-core"}[args.variant],
                     "policy_variant": ags.lora_linear_policy(pool0.handle, n),
                     "distinct_slots_touched": alg["D"], "lora_tokens": alg["n_L"],
+                    "concat_metrics": concat_metrics(idx_np, cases[0].h_in, cases[0].h_out, cases[0].adapters.ranks,
+                                                     cases[0].adapters.r_max, cases[0].adapters.n_slots),
                     "l2": "inputs larger than L2 (no flush)", "timing": "CUDA graph replay, CUDA events",
                     "l2_prefetch_next_weight": prefetch,
                     "calls_per_step": len(calls),
                     "grouped": "projections reading the same x as one call each (lora_linear_fwd_group)" if grouped else None,
                     "parallelism": f"replicas x{world} (token batches sharded across GPUs, no collective)"})
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+                "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f16", "data": "synthetic",
                 "config": cfg, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": int(kernels_per_step) * args.steps, "kernels_per_step": int(kernels_per_step),
+                "gpu_launches": int(kernels_per_step) * steps, "kernels_per_step": int(kernels_per_step),
                 "clocks": clk}
+        return line
+    return None
+
+
+def ours(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    line = measure(args, args.workload, args.steps, args.warmup, world, rank, local, dist, dev, peaks)
+    if args.workload == "decode" and not args.no_prefill_leg:
+        # the metric has two halves: decode against the HBM roofline (the line itself) and
+        # prefill against the tensor roofline (this leg, measured the same way in the same run)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        leg = measure(args, "prefill", min(args.steps, DEFAULT_STEPS["prefill"]), args.warmup, world, rank, local,
+                      dist, dev, peaks)
+        if line is not None:
+            line["prefill"] = {k: leg[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "dtype",
+                                                   "config", "roofline", "cpu_baseline", "e2e", "gpu_launches",
+                                                   "kernels_per_step", "clocks")}
+    if line is not None:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -765,6 +871,218 @@ def adapter_load(args):
             "eager_ms": {"host": ms_host_eager, "device": ms_dev_eager},
             "h2d_memcpy_ms_same_bytes": ms_copy, "h2d_memcpy_GBps": nbytes / (ms_copy * 1e-3) / 1e9,
             "context": "the pages quote 30-80 ms to load a ~30 MB rank-8 adapter over PCIe 5.0 x16"}
+    line["concurrent_with_decode"] = concurrent_mount(args)
+    print(json.dumps(line), flush=True)
+
+
+def concurrent_mount(args):
+    """Decode steps (the headline workload: 64 tokens through 32 q_proj layers) with and without
+    the adapter loader mounting new adapters in the background.
+
+    Every step: the captured decode graph runs on the compute stream and is followed by a
+    release fence on the slots the batch names; meanwhile lora_loader_mount puts k new rank-8
+    adapters (all 32 layers' q_proj pieces, 4 MB each, from pinned host memory) into slots the
+    batch does not name, on the copy stream (one loader call per step) -- the double buffering
+    of the blog.lonae.com page's adapter loader.  Returns ms per step alone and with k = 1 and
+    8 mounts per step."""
+    import numpy as np
+    import torch
+
+    import adapter_gemm_segment_gb300 as ags
+    from adapter_gemm_segment_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    compute, copy = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n, layers, S, R, h = 64, 32, 100, 8, 4096
+    cases = [wl.decode_q_proj(seed=1, n=n, layer=l) for l in range(layers)]
+    idx = cases[0].idx
+    named = sorted(set(idx[idx >= 0].tolist()))
+    free = [sl for sl in range(S) if sl not in set(named)]
+    L = []
+    with torch.cuda.stream(compute):
+        for c in cases:
+            pool = ags.LoraPool(h, h, R, S, c.dtype, dev)
+            L.append({"pool": pool, "W": c.W.to(dev), "x": c.x.to(dev), "y": torch.empty(n, h, dtype=c.dtype, device=dev)})
+        loader = ags.LoraLoader([e["pool"] for e in L], copy)
+        pinned = lambda t: t.contiguous().pin_memory()  # noqa: E731
+        hostA = [pinned(torch.stack(c.adapters.A)) for c in cases]  # one pinned block per layer
+        hostB = [pinned(torch.stack(c.adapters.B)) for c in cases]
+        loader.mount(list(range(S)), [[a[sl] for sl in range(S)] for a in hostA],
+                     [[b[sl] for sl in range(S)] for b in hostB], cases[0].adapters.alphas)
+        loader.acquire(list(range(S)), compute)
+        idx_dev = idx.to(dev)
+        seg_ws = L[0]["pool"].segment_workspace(n, dev)
+        ws = ags._device_bytes(ags.lora_linear_workspace_bytes(L[0]["pool"].handle, n), dev)
+    torch.cuda.synchronize()
+    # the adapters that keep arriving: 16 distinct rank-8 adapters, every layer's q_proj piece
+    rng = np.random.default_rng(77)
+    news = []
+    for k in range(16):
+        ad = wl.draw_adapters(rng, h, h, [R] * layers, [16.0] * layers, torch.float16)
+        Ab, Bb = pinned(torch.stack(ad.A)), pinned(torch.stack(ad.B))
+        news.append(([[Ab[l]] for l in range(layers)], [[Bb[l]] for l in range(layers)]))
+
+    def step():
+        seg = ags.lora_segment(idx_dev, L[0]["pool"].handle, seg_ws, stream=compute)
+        for e in L:
+            ags.lora_linear_fwd(e["pool"].handle, e["W"], e["x"], e["y"], seg, ws, stream=compute)
+
+    with torch.cuda.stream(compute):
+        step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=compute):
+            step()
+    steps = max(50, min(args.steps, 2000))
+
+    def run(k_mounts):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(copy)
+        e0.record(compute)
+        t = 0
+        for i in range(steps):
+            if k_mounts:  # the next k adapters land (one loader call) while this step computes
+                picks = [t + j for j in range(k_mounts)]
+                slots = [free[q % len(free)] for q in picks]
+                As = [[news[q % len(news)][0][l][0] for q in picks] for l in range(layers)]
+                Bs = [[news[q % len(news)][1][l][0] for q in picks] for l in range(layers)]
+                loader.mount(slots, As, Bs, [16.0] * k_mounts)
+                t += k_mounts
+            with torch.cuda.stream(compute):
+                g.replay()
+            loader.release(named, compute)
+        e1.record(compute)
+        c1.record(copy)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps, c0.elapsed_time(c1), t
+
+    alone, _, _ = run(0)
+    out = {"decode_ms_per_step_alone": alone}
+    for k in (1, 8):
+        ms, copy_ms, mounted = run(k)
+        out[f"decode_ms_per_step_with_{k}_mounts"] = ms
+        out[f"mount_GBps_with_{k}_mounts"] = mounted * layers * 2 * (2 * R * h) / (copy_ms * 1e-3) / 1e9
+    # the last mounted adapters are resident and exact: compare one layer's pool slot with its source
+    out["mounts"] = loader.stats()["mounts"]
+    out["config"] = (f"decode 64 tokens x 32 q_proj layers (4096x4096 fp16, 100 slots r=8); per step k new rank-8 "
+                     f"adapters (32 layers x 128 KB each) mounted from pinned host memory on a copy stream into "
+                     f"slots the batch does not name; {steps} steps")
+    loader.close()
+    return out
+
+
+def concat_compare(args):
+    """--workload concat: the segmented path against the concatenated-adapter matmul of the
+    blog.lonae.com page (tensor-concatenation paragraph) on the same decode batches.
+
+    That approach stacks every adapter of the pool (zero-padded to r_max) into A_cat
+    [S*r_max, h_in] and B_cat [h_out, S*r_max], multiplies every token against all of them,
+    keeps each token's own block (scaled by alpha/r) and multiplies back:
+        y = x W^T + ((x A_cat^T) * M) B_cat^T,   M[t, s*r_max + j] = scale_s if idx[t] == s.
+    It runs here as plain cuBLAS GEMMs (torch.matmul) captured in a CUDA graph -- a baseline
+    for comparison, not part of the library.  Both sides run 32 chained decode q_proj linears
+    (4096 x 4096 fp16, 100 rank-8 adapters, Zipf(1.1) + 10 % base-only) per step."""
+    import numpy as np
+    import torch
+
+    import adapter_gemm_segment_gb300 as ags
+    from adapter_gemm_segment_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    layers = args.layers
+    rows = []
+    for n in (1, 8, 64):
+        cases = [wl.decode_q_proj(seed=1, n=n, layer=l) for l in range(layers)]
+        idx = cases[0].idx
+        S, R, h = 100, 8, 4096
+        L = []
+        for c in cases:
+            ad = c.adapters
+            pool = ags.LoraPool(h, h, R, S, c.dtype, dev)
+            for sl in range(S):
+                pool.load_slot(sl, ad.A[sl].to(dev), ad.B[sl].to(dev), ad.alphas[sl])
+            L.append({"pool": pool, "W": c.W.to(dev), "x": c.x.to(dev), "y": torch.empty(n, h, dtype=c.dtype, device=dev),
+                      "yc": torch.empty(n, h, dtype=c.dtype, device=dev), "ad": ad})
+        torch.cuda.synchronize()
+        # the concatenated matrices, from each pool's own zero-padded slabs
+        a_off = 256 * ((S * 16 + 255) // 256)
+        for e in L:
+            mem = e["pool"].mem
+            A_slab = mem[a_off:a_off + S * R * h * 2].view(torch.float16).view(S * R, h)
+            b_off = (a_off + S * R * h * 2 + 255) // 256 * 256
+            B_slab = mem[b_off:b_off + S * h * R * 2].view(torch.float16).view(S, h, R)
+            e["A_cat"] = A_slab
+            e["B_cat"] = B_slab.permute(1, 0, 2).reshape(h, S * R).contiguous()
+        mask = torch.zeros(n, S * R, dtype=torch.float16)
+        for t, sl in enumerate(idx.tolist()):
+            if sl >= 0:
+                mask[t, sl * R:(sl + 1) * R] = L[0]["ad"].alphas[sl] / L[0]["ad"].ranks[sl]
+        mask = mask.to(dev)
+        idx_dev = idx.to(dev)
+        seg_ws = L[0]["pool"].segment_workspace(n, dev)
+        ws = ags._device_bytes(ags.lora_linear_workspace_bytes(L[0]["pool"].handle, n), dev)
+
+        def seg_step():
+            seg = ags.lora_segment(idx_dev, L[0]["pool"].handle, seg_ws)
+            for e in L:
+                ags.lora_linear_fwd(e["pool"].handle, e["W"], e["x"], e["y"], seg, ws)
+
+        def concat_step():
+            for e in L:
+                s_all = torch.matmul(e["x"], e["A_cat"].t())
+                torch.add(torch.matmul(e["x"], e["W"].t()), torch.matmul(s_all * mask, e["B_cat"].t()), out=e["yc"])
+
+        def graph_ms(fn, reps):
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            for _ in range(max(3, args.warmup)):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        reps = max(20, min(args.steps, 500))
+        ms_seg = graph_ms(seg_step, reps)
+        ms_cat = graph_ms(concat_step, reps)
+        # both compute the same layer: the concatenated result must pass the float bar against ours
+        y0, yc0 = L[0]["y"].double().cpu(), L[0]["yc"].double().cpu()
+        agree = bool(((y0 - yc0).abs() <= 1e-2 + 1e-2 * y0.abs()).all())
+        m = concat_metrics(idx.numpy(), h, h, [R] * S, R, S)
+        n_L = int((idx >= 0).sum())
+        rows.append({"tokens": n, "segmented_us_per_linear": 1e3 * ms_seg / layers,
+                     "concat_us_per_linear": 1e3 * ms_cat / layers, "concat_over_segmented": ms_cat / ms_seg,
+                     "lora_flops_segmented": 2 * n_L * R * 2 * h, "lora_flops_concat": 2 * n * S * R * 2 * h,
+                     "concat_lora_flops_wasted_share": m["concat_lora_flops_wasted_share"],
+                     "concat_elements": m["concat_elements"], "concat_projection": m["concat_projection"],
+                     "distinct_adapters": m["distinct_adapters"], "n_segments": m["n_segments"],
+                     "results_agree_within_tolerance": agree})
+        del L, cases
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    line = {"metric": "decode LoRA-linear time: segmented path vs the concatenated-adapter matmul",
+            "value": rows[-1]["segmented_us_per_linear"], "unit": "us per linear", "higher_is_better": False,
+            "n_gpus": 1, "steps": max(20, min(args.steps, 500)), "warmup": max(3, args.warmup), "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": f"decode q_proj 4096x4096 fp16, {layers} chained layers per step, 100 adapters "
+                                   "r=8 alpha=16, Zipf(1.1) + 10% base-only; batches of 1, 8 and 64 tokens",
+                       "concat_impl": "cuBLAS GEMMs through torch.matmul in a CUDA graph (baseline only)",
+                       "timing": "CUDA graph replay, CUDA events"},
+            "rows": rows}
     print(json.dumps(line), flush=True)
 
 
@@ -772,6 +1090,8 @@ def main():
     args = parse_args()
     if args.workload == "load":
         adapter_load(args)
+    elif args.workload == "concat":
+        concat_compare(args)
     elif args.impl == "reference":
         reference_arm(args)
     else:

@@ -311,6 +311,41 @@ int lora_cache_stats(lora_cache_t cache, uint64_t* hits, uint64_t* misses, uint6
  * (device float32, n <= 2^20) is set to 1.0 and *status_dev is left as it was. */
 int lora_wait_selftest(int32_t* status_dev, float* out_dev, int n, int arrive, uint64_t limit_ns, void* stream);
 
+/* ---- adapter loader: background mounts on a copy stream, draining remounts -------------
+ *
+ * The blog.lonae.com page's adapter loader fills the execution unit's buffers without
+ * blocking inference: asynchronous double buffering -- one copy serves the running requests
+ * while the next candidate adapter is fetched in the background from pinned host memory.  The
+ * xpshop.cn article 492 (section 三) unloads adapters in "draining" mode: requests already
+ * running on an adapter finish before it goes.  A loader manages `count` pools with the same
+ * n_slots (the projections an adapter targets; slot s of every pool holds the same adapter)
+ * and a copy stream owned by the caller.  Ordering is by CUDA events, with no host
+ * synchronisation:
+ *   lora_loader_mount: enqueue, on the copy stream, mounts of adapters into `count` distinct
+ *     slots.  Entry (p, i) = A[p*count + i], B[p*count + i], ranks[...], alphas[...] is slot
+ *     slots[i]'s adapter for pool p, with the meaning of lora_pool_load_slots (A/B in pinned
+ *     host memory, read by the mount kernel; kept valid by the caller until the copy stream
+ *     has passed the mount).  A slot that holds an adapter is drained first: the copy stream
+ *     waits for every fence lora_loader_release recorded on it since its last mount, then the
+ *     slot is unmounted and remounted.  Everything is validated before anything is enqueued
+ *     (LORA_ESLOT, LORA_ERANK, LORA_EBUSY for a slot named twice, LORA_EINVAL).
+ *   lora_loader_acquire: make `stream` wait until the latest mount of each named slot has
+ *     landed (call it before segmenting a batch that names a freshly mounted slot).
+ *   lora_loader_release: record on `stream` a fence after the work enqueued so far, which may
+ *     read the named slots; a later remount of any of them waits for it.  Release every slot
+ *     a batch names after that batch's linears.
+ *   lora_loader_stats: slots mounted so far, fences drained by remounts.
+ * The loader's pools must be mounted and unmounted only through it, and must outlive it.
+ * Not thread-safe. */
+typedef struct lora_loader* lora_loader_t;
+int lora_loader_create(int count, const lora_pool_t* pools, void* copy_stream, lora_loader_t* out);
+int lora_loader_destroy(lora_loader_t loader);
+int lora_loader_mount(lora_loader_t loader, int count, const int* slots, const void* const* A, const void* const* B,
+                      const int* ranks, const float* alphas);
+int lora_loader_acquire(lora_loader_t loader, int count, const int* slots, void* stream);
+int lora_loader_release(lora_loader_t loader, int count, const int* slots, void* stream);
+int lora_loader_stats(lora_loader_t loader, uint64_t* mounts, uint64_t* drained_fences);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* lora_last_error(void);
 

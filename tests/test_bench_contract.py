@@ -40,3 +40,21 @@ def test_host_only_package_users_do_not_map_the_library():
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     assert out.stdout.strip().splitlines()[-1] == "False"
+
+
+def test_concat_metrics_by_hand():
+    """The tensor-concatenation figures of the benchmark line on a hand-worked batch:
+    idx = [-1, 0, 0, 2] over 3 slots of ranks 8, 16, 4 padded to r_max 16, h_in 10, h_out 6."""
+    m = bench.concat_metrics([-1, 0, 0, 2], 10, 6, [8, 16, 4], 16, 3)
+    assert m["n_segments"] == 3 and m["distinct_adapters"] == 2  # runs -1, 0, 2
+    assert m["concat_elements"] == 3 * 16 * (10 + 6) == 768
+    assert m["concat_projection"] == [4, 48] and m["concat_projection_elements"] == 192
+    # tokens 0, 0, 2 at r_max 16 multiply 8 + 8 + 12 padded rows out of 48
+    assert abs(m["zero_pad_flop_share"] - 28 / 48) < 1e-15
+    # touched adapters 0 and 2 store 8 + 12 padded rows out of 32
+    assert abs(m["zero_pad_stored_share"] - 20 / 32) < 1e-15
+    # concatenated LoRA FLOPs 2*4*48*16 = 6144, of which the 3 LoRA tokens' own blocks 2*3*16*16 = 1536
+    assert abs(m["concat_lora_flops_wasted_share"] - 0.75) < 1e-15
+    empty = bench.concat_metrics([-1, -1], 10, 6, [8], 8, 1)
+    assert empty["n_segments"] == 1 and empty["zero_pad_flop_share"] == 0.0
+    assert empty["concat_lora_flops_wasted_share"] == 1.0
