@@ -36,7 +36,7 @@ EXPORTED = (
     "lora_set_timing_events", "lora_linear_fwd_static_ws", "lora_linear_fwd_ex", "lora_pool_load_slots",
     "lora_linear_group_workspace_bytes", "lora_linear_fwd_group", "lora_linear_group_policy",
     "lora_cache_create", "lora_cache_destroy", "lora_cache_register", "lora_cache_unregister", "lora_cache_map",
-    "lora_cache_slot_of", "lora_cache_stats", "lora_wait_selftest", "lora_set_kernel_stamps",
+    "lora_cache_slot_of", "lora_cache_stats", "lora_wait_selftest", "lora_set_kernel_stamps", "lora_set_aux_stamps",
     "lora_loader_create", "lora_loader_destroy", "lora_loader_mount", "lora_loader_acquire", "lora_loader_release",
     "lora_loader_stats",
 )
@@ -94,6 +94,7 @@ def _load() -> ctypes.CDLL:
         "lora_cache_stats": [vp, P(ctypes.c_uint64), P(ctypes.c_uint64), P(ctypes.c_uint64)],
         "lora_wait_selftest": [vp, vp, i32, i32, ctypes.c_uint64, vp],
         "lora_set_kernel_stamps": [vp, i32],
+        "lora_set_aux_stamps": [vp, i32],
         "lora_loader_create": [i32, P(vp), vp, P(vp)],
         "lora_loader_destroy": [vp],
         "lora_loader_mount": [vp, i32, P(i32), P(vp), P(vp), P(i32), P(ctypes.c_float)],
@@ -159,6 +160,18 @@ def lora_set_kernel_stamps(stamps: Optional[torch.Tensor] = None) -> None:
     if stamps.dtype != torch.int64 or stamps.dim() != 2 or stamps.shape[1] != 2 or not stamps.is_contiguous():
         raise ValueError("stamps must be a contiguous int64 tensor of shape [pairs, 2]")
     _check(_lib.lora_set_kernel_stamps(_ptr(_dev(stamps, "stamps")), int(stamps.shape[0])))
+
+
+def lora_set_aux_stamps(stamps: Optional[torch.Tensor] = None) -> None:
+    """While set (a device int64 tensor [triples, 3]), every shrink / segmented-expand launch of
+    the decode path records {first CTA start, first grid-dependency wait return, last CTA end}
+    (%globaltimer ns) into the next triple; initialise to (-1, -1, 0).  No argument disables."""
+    if stamps is None:
+        _check(_lib.lora_set_aux_stamps(ctypes.c_void_p(0), 0))
+        return
+    if stamps.dtype != torch.int64 or stamps.dim() != 2 or stamps.shape[1] != 3 or not stamps.is_contiguous():
+        raise ValueError("stamps must be a contiguous int64 tensor of shape [triples, 3]")
+    _check(_lib.lora_set_aux_stamps(_ptr(_dev(stamps, "stamps")), int(stamps.shape[0])))
 
 
 def lora_wait_selftest(status: torch.Tensor, out: torch.Tensor, arrive: bool, limit_ns: int, stream=None) -> None:

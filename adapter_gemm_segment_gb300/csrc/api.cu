@@ -32,6 +32,17 @@ static unsigned long long* g_stamps = nullptr;
 static int g_stamp_pairs = 0;
 static int g_stamp_next = 0;
 
+static unsigned long long* g_aux = nullptr;
+static int g_aux_triples = 0;
+static int g_aux_next = 0;
+
+unsigned long long* take_aux_stamp() {
+    if (!g_aux || g_aux_triples <= 0) return nullptr;
+    unsigned long long* p = g_aux + 3 * (size_t)g_aux_next;
+    g_aux_next = (g_aux_next + 1) % g_aux_triples;
+    return p;
+}
+
 unsigned long long* take_kernel_stamp() {
     if (!g_stamps || g_stamp_pairs <= 0) return nullptr;
     unsigned long long* p = g_stamps + 2 * (size_t)g_stamp_next;
@@ -108,6 +119,15 @@ extern "C" {
 const char* lora_last_error(void) { return g_err; }
 
 uint64_t lora_kernel_launch_count(void) { return g_launches.load(); }
+
+int lora_set_aux_stamps(void* stamps_dev, int triples) {
+    if (stamps_dev && triples <= 0) return set_error(LORA_EINVAL, "triples must be > 0");
+    if (reinterpret_cast<uintptr_t>(stamps_dev) % 8) return set_error(LORA_EINVAL, "stamps must be 8-byte aligned");
+    g_aux = static_cast<unsigned long long*>(stamps_dev);
+    g_aux_triples = stamps_dev ? triples : 0;
+    g_aux_next = 0;
+    return LORA_OK;
+}
 
 int lora_set_kernel_stamps(void* stamps_dev, int pairs) {
     if (stamps_dev && pairs <= 0) return set_error(LORA_EINVAL, "pairs must be > 0");

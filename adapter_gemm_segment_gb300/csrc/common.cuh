@@ -96,6 +96,7 @@ struct GroupView {
     const void* B[kMaxGroup];
     long long s_stride;  // floats between the shrink outputs of consecutive slices
     int rank_aware;      // some mounted slot holds a rank below r_max: kernels may skip its padding
+    unsigned long long* stamp;  // benchmark instrumentation of the launch (nullptr: off)
 };
 
 // Whether some slot of the pool (empty slots count at r_max) holds fewer 8-column chunks than
@@ -177,6 +178,21 @@ __device__ __forceinline__ void stamp_start(unsigned long long* st) {
 __device__ __forceinline__ void stamp_end(unsigned long long* st) {
     if (st != nullptr && threadIdx.x == 0) atomicMax(st + 1, stamp_clock());
 }
+// The shrink / expand kernels' stamps (lora_set_aux_stamps): a triple {first CTA start, first
+// return from the grid-dependency wait, last CTA end}, the end taken when thread 0 leaves.
+unsigned long long* take_aux_stamp();
+struct AuxStamp {
+    unsigned long long* p;
+    __device__ explicit AuxStamp(unsigned long long* q) : p(q) {
+        if (p != nullptr && threadIdx.x == 0) atomicMin(p, stamp_clock());
+    }
+    __device__ void waited() const {
+        if (p != nullptr && threadIdx.x == 0) atomicMin(p + 1, stamp_clock());
+    }
+    __device__ ~AuxStamp() {
+        if (p != nullptr && threadIdx.x == 0) atomicMax(p + 2, stamp_clock());
+    }
+};
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

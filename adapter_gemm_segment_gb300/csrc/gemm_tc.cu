@@ -588,6 +588,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     }
 
     // ---- phase D: late LoRA groups, reduction over the cluster, store ----
+    // The closing cluster barrier keeps every CTA alive until the copies out of its parked rows
+    // have landed.  With pushed partials, a CTA's incoming copies are complete once its receive
+    // barrier fires, so its epilogue threads announce their arrival right then and only wait
+    // at the very end: the barrier's latency overlaps the reduction and the y store.
+    bool arrived = false;
     if (warp >= 2 && flags[1]) {
         float* own = P + (size_t)t0 * BM;  // this CTA's partials of its own tokens (LoRA added here)
         const int D = flags[2];
@@ -642,6 +647,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         bool recv = true;
         if (push && cnt > 0 && a.splits > 1) recv = __all_sync(0xffffffffu, mbar_wait(rbar, 0, flags));
+        if (push) {
+            cluster_arrive();
+            arrived = true;
+        }
         // y is assembled in shared memory 32 tokens at a time (two buffers of [32][128], after
         // the receive buffer) and written with TMA stores; rows/columns outside y are clipped
         T* Ysm = smem_align(reinterpret_cast<T*>(Rcv + (push ? (size_t)(a.splits - 1) * per * BM : 0)), 128);
@@ -712,7 +721,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         if (et == 0) bulk_wait_group_read0();
     }
     tc_fence_before();
-    cluster_sync();  // no CTA leaves while its parked rows may still be copied or read
+    if (!arrived) cluster_arrive();
+    cluster_wait();  // no CTA leaves while its parked rows may still be copied or read
     if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
     stamp_end(a.stamp);
 }

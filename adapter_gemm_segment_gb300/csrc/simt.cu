@@ -86,7 +86,9 @@ shrink_token_kernel(PoolView pool, GroupView grp, SegView seg, const T* __restri
     __shared__ float red[4][8];
     // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
     // every kernel before this one has completed (x, W) and waits separately for s.
+    AuxStamp stamp(grp.stamp);
     pdl_wait();
+    stamp.waited();
     pdl_trigger();
     const int t = blockIdx.x, ks = blockIdx.z;
     const int h = pool.h_in, R = pool.R, rg = R / 8;
@@ -160,7 +162,9 @@ shrink_seg_kernel(PoolView pool, GroupView grp, SegView seg, const T* __restrict
     __shared__ float red[4][32];
     // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
     // every kernel before this one has completed (x, W) and waits separately for s.
+    AuxStamp stamp(grp.stamp);
     pdl_wait();
+    stamp.waited();
     pdl_trigger();
     const int b = blockIdx.x, ks = blockIdx.z;
     const int h = pool.h_in, R = pool.R, rg = R / 8;
@@ -406,7 +410,9 @@ __global__ void __launch_bounds__(256)
 expand_seg_kernel(PoolView pool, GroupView grp, SegView seg, const float* __restrict__ s_in, int s_parts,
                   T* __restrict__ y, int fpt) {
     extern __shared__ float ss[];  // [4][R]: the item's shrink rows (K parts summed)
+    AuxStamp stamp(grp.stamp);
     pdl_wait();
+    stamp.waited();
     pdl_trigger();
     const int b = blockIdx.x;
     // grid columns: expand blocks (256 * fpt features) of the group's slices, one after another
@@ -556,7 +562,9 @@ static int launch_shrink_t(const PoolView& pv, const GroupView& grp, const SegVi
     if constexpr (sizeof(T) == 2) {
         if (!tiled) {
             if (sv.n == 0) return LORA_OK;
-            void* args[] = {(void*)&pv, (void*)&grp, (void*)&sv, (void*)&xp, (void*)&s_out};
+            GroupView g1 = grp;
+            g1.stamp = take_aux_stamp();
+            void* args[] = {(void*)&pv, (void*)&g1, (void*)&sv, (void*)&xp, (void*)&s_out};
             const int rows = grp.count * (pv.R / 8);  // (slice, 8-row group) pairs
             // Per token, every LoRA token re-reads its adapter's A rows: n * r_max * h_in * 2
             // bytes at most.  Past 16 MB (r_max 64 at 64 tokens, 4096 features: 33.5 MB) the
@@ -625,6 +633,7 @@ static int launch_expand_t(const PoolView& pv, const GroupView& grp, const SegVi
         const int items = std::min(sv.n, std::min(sv.n, pv.S) + (sv.n + kItemTok - 1) / kItemTok);
         // two features per thread when the grid keeps two CTAs per SM that way
         GroupView g2 = grp;
+        g2.stamp = take_aux_stamp();
         int blocks512 = 0;
         for (int q = 0; q < grp.count; ++q) blocks512 += (grp.col[q + 1] - grp.col[q] + 511) / 512;
         const int fpt = (long long)items * blocks512 >= 2LL * num_sms() ? 2 : 1;

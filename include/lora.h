@@ -370,6 +370,13 @@ int lora_set_timing_events(void* before_shrink, void* before_gemm, void* after_g
  * disables.  LORA_EINVAL for pairs <= 0 with a buffer, or a misaligned buffer. */
 int lora_set_kernel_stamps(void* stamps_dev, int pairs);
 
+/* The same for the CUDA-core shrink and segmented-expand kernels of the decode path: while set,
+ * each of their launches takes the next of `triples` triples of uint64 (round robin, restarting
+ * at triple 0 on every call of this function) and records {first CTA start (atomicMin),
+ * first return from its grid-dependency wait (atomicMin), last CTA end (atomicMax; thread 0's
+ * exit)}; initialise triples to {UINT64_MAX, UINT64_MAX, 0}.  NULL disables. */
+int lora_set_aux_stamps(void* stamps_dev, int triples);
+
 #ifdef __cplusplus
 }
 #endif
