@@ -197,23 +197,43 @@ int lora_linear_fwd_ex(lora_pool_t pool, const void* W_dev, const void* x_dev, v
     if (ws_bytes < L.total) return set_error(LORA_ENOSPACE, "linear workspace needs %zu bytes, got %zu", L.total, ws_bytes);
     char* w = static_cast<char*>(ws_dev);
     float* s_buf = reinterpret_cast<float*>(w + L.s_off);
+    return linear_fwd_impl(pool, W_dev, x_dev, y_dev, seg, variant, s_buf, prefetch_dev, prefetch_bytes,
+                           static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace lora {
+
+// The launch sequence of one LoRA-augmented linear, after its arguments were checked; s_buf
+// receives the shrink output (float32 [parts][n][r_max]).
+int linear_fwd_impl(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev, const lora_segments* seg,
+                    int variant, float* s_buf, const void* prefetch_dev, size_t prefetch_bytes, cudaStream_t st) {
+    const PoolView pv = pool_view(pool);
+    const int n = seg->n_tokens;
     if (variant == LORA_VARIANT_AUTO) lora_linear_policy(pool, n, &variant);
     const SegView sv = seg_view(seg);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     const bool tc = variant != kVariantCudaCore && tc_supported(pv, n);
     const bool fused = variant != LORA_VARIANT_SEPARATE;
+    // Fused decode batches compute the shrink inside the base GEMM's grid when that grid fits on
+    // the GPU at once: no shrink kernel, so each linear's GEMM follows the previous kernel
+    // directly (one dependency hop per linear instead of two).
+    const bool grid_shrink = tc && fused && n <= 256 && decode_grid_shrink_ok(pv, n);
     record_if(g_ev_before_shrink, st);
-    int rc;
+    int rc = LORA_OK;
     int s_parts = 1;
-    if (tc && n > 256 && shrink_tc_supported(pv))
+    if (grid_shrink)
+        s_parts = shrink_parts(pv, n, false);
+    else if (tc && n > 256 && shrink_tc_supported(pv))
         rc = launch_shrink_tc(pv, sv, x_dev, s_buf, st);
     else
         rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256, &s_parts);
     if (rc) return rc;
     record_if(g_ev_before_gemm, st);
     if (tc) {
-        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st, prefetch_dev, prefetch_bytes);
+        rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st, prefetch_dev, prefetch_bytes,
+                            nullptr, grid_shrink);
     } else {
         rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
     }
@@ -226,7 +246,7 @@ int lora_linear_fwd_ex(lora_pool_t pool, const void* W_dev, const void* x_dev, v
     return LORA_OK;
 }
 
-}  // extern "C"
+}  // namespace lora
 
 // ---- grouped projections ------------------------------------------------------------------
 

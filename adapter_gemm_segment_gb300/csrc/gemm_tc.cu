@@ -27,6 +27,9 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -64,6 +67,13 @@ struct DecodeArgs {
     const char* prefetch;  // optional range streamed into L2 once this CTA's accumulator is complete
     size_t prefetch_bytes;
     unsigned long long* stamp;  // benchmark instrumentation (nullptr: off)
+    // In-grid shrink: no shrink kernel precedes this grid.  After the grid-dependency wait the
+    // epilogue warps of every CTA compute the shrink's work units into s_out (== s_in) and hand
+    // it over through ctr = {produced, consumed} (in the segment workspace, zero on entry).
+    int grid_shrink;
+    const void* x;  // [n, h_in], read directly by the in-grid shrink
+    float* s_out;
+    int* ctr;
 };
 
 struct PrefillArgs {
@@ -250,6 +260,88 @@ __device__ __forceinline__ void lora_batch8_pre(const uint4* __restrict__ Bp4, c
 //          CTA owns into that CTA's receive buffer (completion on the receiver's mbarrier); when
 //          the buffers do not fit, owners read the partials remotely instead.
 //  phase D: owners add the partials, the LoRA term and store y.  No global scratch.
+// In-grid shrink of the decode GEMM.  The work units of the segmented shrink -- (work item = up
+// to 4 sorted tokens of one adapter, 8-row group of r_max, K part) -- are dealt round robin over
+// the CTAs of the grid (CTA cta of n_ctas), and the 128 epilogue threads of a CTA compute one
+// unit together, as one CTA of the separate shrink kernel does: 8 features per thread and
+// sweep, so a part of up to 1024 features costs one round trip to memory.  A thread's 4 x 8
+// partial dot products (tokens x adapter rows) are reduced over its warp (reduce-scatter
+// butterfly: lane L ends with sum L = token L/8, row L%8), then over the 4 warps through red
+// [4][32], and scale * sum goes to s_out[(part * n + token) * r_max + row].  Row groups past the
+// adapter's true rank store zeros, as the separate shrink kernel does.
+template <typename T>
+__device__ __forceinline__ void grid_shrink_units(const DecodeArgs& a, int cta, int n_ctas, int et, float* red) {
+    const int lane = et & 31, w = et >> 5;
+    const int R = a.pool.R, h = a.pool.h_in, rg = R / 8, parts = a.s_parts, n = a.n;
+    const int n_items = __ldcg(a.seg.nseg + 1);
+    const int units = n_items * rg * parts;
+    const T* __restrict__ x = static_cast<const T*>(a.x);
+    const T* __restrict__ A = static_cast<const T*>(a.pool.A);
+    const int sweeps = ((h + 1023) / 1024 + parts - 1) / parts;  // the shrink kernels' K-part split
+    for (int u = cta; u < units; u += n_ctas) {
+        const int b = u / (rg * parts);
+        const int rem = u - b * rg * parts;
+        const int g = rem / parts, ks = rem - g * parts;
+        const int4 head = __ldcg(reinterpret_cast<const int4*>(a.seg.items + (size_t)b * 8));  // slot, count, tok0, tok1
+        const int4 tail = __ldcg(reinterpret_cast<const int4*>(a.seg.items + (size_t)b * 8 + 4));  // tok2, tok3, rank
+        const int slot = head.x, nt = head.y;
+        const int tok[4] = {head.z, head.w, tail.x, tail.y};
+        if (g * 8 >= tail.z && g * 8 >= a.pool.table[slot].rank) {  // rows past the true rank: A is zero
+            if (et < nt * 8) {
+                const int q = et >> 3;
+                const int t = q == 0 ? head.z : q == 1 ? head.w : q == 2 ? tail.x : tail.y;
+                a.s_out[((size_t)ks * n + t) * R + g * 8 + (et & 7)] = 0.f;
+            }
+            continue;  // uniform over the CTA: the condition depends on the unit only
+        }
+        const int k_beg = ks * sweeps * 1024;
+        const int k_end = min(h, k_beg + sweeps * 1024);
+        const T* Ab = A + ((size_t)slot * R + (size_t)g * 8) * h;
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        for (int k = k_beg + et * 8; k < k_end; k += 1024) {
+            uint4 av[8], xv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xv[q] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)tok[q] * h + k));
+#pragma unroll
+            for (int r = 0; r < 8; ++r) av[r] = __ldg(reinterpret_cast<const uint4*>(Ab + (size_t)r * h + k));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float xf[8];
+                unpack8<T>(xv[q], xf);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    float af[8];
+                    unpack8<T>(av[r], af);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[q * 8 + r] = fmaf(xf[e], af[e], v[q * 8 + r]);
+                }
+            }
+        }
+#pragma unroll
+        for (int step = 0; step < 5; ++step) {
+            const int half = 16 >> step, off = 16 >> step;
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int e = 0; e < half; ++e) {
+                const float send = up ? v[e] : v[e + half];
+                const float keepv = up ? v[e + half] : v[e];
+                v[e] = keepv + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+        red[w * 32 + lane] = v[0];
+        named_bar_sync(1, 128);
+        if (et < nt * 8) {
+            const int q = et >> 3;
+            const int t = q == 0 ? head.z : q == 1 ? head.w : q == 2 ? tail.x : tail.y;
+            const float sum = red[et] + red[32 + et] + red[64 + et] + red[96 + et];
+            a.s_out[((size_t)ks * n + t) * R + g * 8 + (et & 7)] = a.pool.table[slot].scale * sum;
+        }
+        named_bar_sync(1, 128);  // red is reused by the next unit
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -272,7 +364,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int* dlist = dloc_sm + per;                                                 // [per]
     int* fidx_sm = dlist + per;                                                 // [per]
     int* pre_sm = fidx_sm + per;  // [1 + 2 kMaxPre]: staged slots; their uint4 offsets; chunks per row
-    float* S_sm = smem_align(reinterpret_cast<float*>(pre_sm + 1 + 2 * kMaxPre), 16);  // [s_parts][per][R]
+    float* red_sm = reinterpret_cast<float*>(pre_sm + 1 + 2 * kMaxPre);  // [4][32]: in-grid shrink reduction
+    float* S_sm = smem_align(red_sm + 128, 16);  // [s_parts][per][R]
     float* L_sm = S_sm + (size_t)a.s_parts * per * R;                            // [per][128] if use_lsm
     T* Bpre = smem_align(reinterpret_cast<T*>(L_sm + (use_lsm ? (size_t)per * BM : 0)), 128);  // bpre_bytes
     uint64_t* full = smem_align(reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(Bpre) + a.bpre_bytes), 8);
@@ -302,20 +395,32 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const bool push = a.push != 0;
 
     // stage i of this CTA's K walk: its W box and x box, counted on full[i % stages]
-    auto issue_stage = [&](int i) {
+    auto issue_w = [&](int i) {  // expects the whole stage, loads its W box
         const int s = i % stages;
         const int kb = kb0 + ((i + kb_rot) % nkb) * kc;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
-        if (kc == 1) {
+        if (kc == 1)
             tma_load_2d_cta(smem + s * stage_bytes, &tmW, &full[s], kb * BK, m_tile * BM);
-            tma_load_2d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], kb * BK, 0);
-        } else {
+        else
             tma_load_3d_cta(smem + s * stage_bytes, &tmW, &full[s], 0, m_tile * BM, kb);
+    };
+    auto issue_x = [&](int i) {
+        const int s = i % stages;
+        const int kb = kb0 + ((i + kb_rot) % nkb) * kc;
+        if (kc == 1)
+            tma_load_2d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], kb * BK, 0);
+        else
             tma_load_3d_cta(smem + s * stage_bytes + w_bytes, &tmX, &full[s], 0, 0, kb);
-        }
+    };
+    auto issue_stage = [&](int i) {
+        issue_w(i);
+        issue_x(i);
     };
     // The producer thread initialises the barriers and fills the ring right away, so the first
-    // HBM round trip overlaps the TMEM allocation and the CTA-wide barrier below.
+    // HBM round trip overlaps the TMEM allocation and the CTA-wide barrier below.  With the
+    // in-grid shrink no kernel between the previous one and this grid has waited for it, so only
+    // the W boxes go out now (a weight is never written by the kernel just before the linear);
+    // the x boxes follow the grid-dependency wait.
     const int pre = min(stages, nkb);
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -329,7 +434,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         fence_barrier_init();
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
-        for (int i = 0; i < pre; ++i) issue_stage(i);
+        for (int i = 0; i < pre; ++i) {
+            if (a.grid_shrink)
+                issue_w(i);
+            else
+                issue_stage(i);
+        }
         prefetch_tmap(&tmY);
         prefetch_tmap(&tmYtail);
         if (a.compact && a.fuse) prefetch_tmap(&tmB);
@@ -351,10 +461,16 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const T* B = static_cast<const T*>(a.pool.B);
 
     if (warp == 0) {
-        // W and x are complete when this grid starts: the shrink kernel that precedes it in the
-        // stream releases its dependents only after its own grid-dependency wait.  Only the
-        // shrink output (read by the epilogue warps) needs this grid's wait.
+        // W and x are complete when this grid starts if a shrink kernel precedes it in the
+        // stream: it releases its dependents only after its own grid-dependency wait, and only
+        // the shrink output (read by the epilogue warps) needs this grid's wait.  With the
+        // in-grid shrink this grid follows the previous kernel directly and waits itself before
+        // the first x box.
         if (lane == 0) {
+            if (a.grid_shrink) {
+                pdl_wait();
+                for (int i = 0; i < pre; ++i) issue_x(i);
+            }
             int issued = pre;  // stages 0 .. pre-1 went out before the CTA-wide barrier
             for (int i = pre; i < nkb; ++i) {
                 const int s = i % stages;
@@ -399,10 +515,48 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
     } else {
         // ---- phase A (overlaps the main loop): stage this CTA's LoRA operands ----
-        pdl_wait();  // s, idx and the status word come from earlier kernels
+        pdl_wait();  // s (or x for the in-grid shrink), idx and the status word come from earlier kernels
         if (et == 0) flags[3] = __ldcg(a.seg.status);
         named_bar_sync(1, 128);
+        const int n_ctas = gridDim.x * gridDim.y;
+        // In-grid shrink: every CTA computes its share of the shrink units, then counts itself
+        // produced -- also with nothing to do or an error status, so that the hand-off always
+        // completes.  The output is complete once every CTA has counted itself produced
+        // (bounded wait: on timeout the status word says so and y is not written).  Then the
+        // CTA counts itself consumed; the last one resets both counters for the next linear.
+        auto wait_produced = [&]() {
+            if (et == 0) {
+                const unsigned long long t0w = globaltimer();
+                int got = 0;
+                while ((got = ld_acquire_gpu(&a.ctr[0])) < n_ctas) {
+                    if (globaltimer() - t0w > kWaitLimitNs) break;
+                    __nanosleep(64);
+                }
+                if (got < n_ctas) {
+                    flags[0] = 1;
+                    report_timeout_status(a.seg.status);
+                }
+            }
+            named_bar_sync(1, 128);
+        };
+        auto consume = [&]() {
+            if (et == 0 && atomicAdd(&a.ctr[1], 1) == n_ctas - 1) {
+                atomicExch(&a.ctr[0], 0);
+                atomicExch(&a.ctr[1], 0);
+            }
+        };
+        auto produce = [&](bool work) {
+            if (work) grid_shrink_units<T>(a, blockIdx.y * gridDim.x + blockIdx.x, n_ctas, et, red_sm);
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (et == 0) atomicAdd(&a.ctr[0], 1);
+        };
         const bool lora = flags[3] == LORA_OK && a.fuse;
+        if (!lora && a.grid_shrink) {
+            produce(false);
+            wait_produced();
+            consume();
+        }
         if (lora) {
             for (int q = et; q < cnt; q += 128) slot_sm[q] = __ldcg(a.seg.idx + t0 + q);
             named_bar_sync(1, 128);
@@ -463,10 +617,12 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         ++ns;
                     }
                     pre_sm[0] = ns;
-                    // bulk copies of the owned tokens' shrink parts, then one TMA box per staged
-                    // slot and 8-column chunk: [128 feature rows][8 columns] of B
-                    mbar_arrive_expect_tx(lbar, (cnt > 0 ? a.s_parts * s_bytes : 0) + static_cast<uint32_t>(off) * 16);
-                    if (cnt > 0)
+                    // bulk copies of the owned tokens' shrink parts (unless the in-grid shrink
+                    // is still writing them), then one TMA box per staged slot and 8-column
+                    // chunk: [128 feature rows][8 columns] of B
+                    const uint32_t sb = (cnt > 0 && !a.grid_shrink) ? a.s_parts * s_bytes : 0;
+                    mbar_arrive_expect_tx(lbar, sb + static_cast<uint32_t>(off) * 16);
+                    if (sb)
                         for (int k = 0; k < a.s_parts; ++k)
                             bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
                     uint4* Bp4 = reinterpret_cast<uint4*>(Bpre);
@@ -479,8 +635,9 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint32_t b_bytes = static_cast<uint32_t>(rows_valid * R * 2);
                     const int ns = min(min(running, kMaxPre), a.bpre_bytes / (BM * R * 2));
                     pre_sm[0] = ns;
-                    mbar_arrive_expect_tx(lbar, (cnt > 0 ? a.s_parts * s_bytes : 0) + ns * b_bytes);
-                    if (cnt > 0)
+                    const uint32_t sb = (cnt > 0 && !a.grid_shrink) ? a.s_parts * s_bytes : 0;
+                    mbar_arrive_expect_tx(lbar, sb + ns * b_bytes);
+                    if (sb)
                         for (int k = 0; k < a.s_parts; ++k)
                             bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
                     for (int d = 0; d < ns; ++d)
@@ -489,6 +646,16 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 }
             }
             named_bar_sync(1, 128);
+            if (a.grid_shrink) {  // this CTA's shrink share; the owned tokens' parts once the grid is done
+                produce(true);
+                wait_produced();
+                for (int e = et; e < a.s_parts * cnt * R; e += 128) {
+                    const int k = e / (cnt * R), r = e - k * cnt * R;
+                    S_sm[(size_t)k * per * R + r] = __ldcg(a.s_in + ((size_t)k * n + t0) * R + r);
+                }
+                named_bar_sync(1, 128);
+                consume();
+            }
             const int Dg = pre_sm[0];
             const bool staged = mbar_wait(lbar, 0, flags);
             // sum the shrink's K-parts once (part 0 receives the total)
@@ -1110,7 +1277,7 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     const bool use_lsm = per <= kLsmMaxTokens;
     // dedicated region: 4 int arrays, the staged-slot table, s parts [s_parts][per][R], LoRA
     // term [per][128] (small shares), alignment, barriers
-    const size_t fixed = (size_t)per * 4 * 4 + (1 + 2 * kMaxPre) * 4 + 16 + (size_t)s_parts * per * pv.R * 4 +
+    const size_t fixed = (size_t)per * 4 * 4 + (1 + 2 * kMaxPre) * 4 + 128 * 4 + 16 + (size_t)s_parts * per * pv.R * 4 +
                          (use_lsm ? (size_t)per * BM * 4 : 0) + 128 + 2 * 1024;
     const size_t slot_b = (size_t)BM * pv.R * 2;  // one B tile at r_max (the late path's unit)
     // B tiles staged during the main loop are kept at their slots' true ranks: k slots need at
@@ -1179,10 +1346,62 @@ int decode_fused_fits(const PoolView& pv, int n) {
     return per <= tc::kLsmMaxTokens && p.dpre >= std::min(per, pv.S) ? 1 : 0;
 }
 
+// Clusters of the decode kernel (one CTA per SM at its shared-memory size) that the GPU holds
+// at once, for a cluster of `splits` CTAs (queried once per shape).
+static int decode_max_clusters(const tc::DecodePlan& p) {
+    static std::mutex mu;
+    static std::vector<std::pair<std::pair<size_t, int>, int>> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& c : cache)
+        if (c.first.first == p.smem && c.first.second == p.splits) return c.second;
+    int clusters = 0;
+    if (cudaFuncSetAttribute(tc::gemm_decode_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
+        cudaSuccess) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(p.m_tiles, p.splits);
+        cfg.blockDim = dim3(tc::kThreads);
+        cfg.dynamicSmemBytes = p.smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = p.splits;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)tc::gemm_decode_kernel<__half>, &cfg) != cudaSuccess)
+            clusters = 0;
+    }
+    (void)cudaGetLastError();  // a refused query only disables the in-grid shrink
+    cache.push_back({{p.smem, p.splits}, clusters});
+    return clusters;
+}
+
+// Measured on GB300 (32 chained 4096 x 4096 fp16 linears, 100 rank-8 adapters, one box, us per
+// linear with the in-grid shrink / with the shrink kernel): 1 token 12.04 / 13.43, 2: 12.35 /
+// 13.49, 4: 12.60 / 13.62, 8: 12.83 / 13.62, 16: 14.22 / 14.01, 32: 14.83 / 14.46, 64: 15.63 /
+// 14.90.  From 16 tokens on, the hand-off of the shrink output between the grid's CTAs costs
+// more than the shrink kernel's extra dependency hop.
+constexpr int kGridShrinkMaxTokens = 8;
+
+int decode_grid_shrink_ok(const PoolView& pv, int n) {
+    if (n <= 0 || n > kGridShrinkMaxTokens || !tc_supported(pv, n)) return 0;
+    const int parts = shrink_parts(pv, n, false);
+    const tc::DecodePlan p = tc::plan_decode(pv, n, parts);
+    // Its work units (at most one shrink item per LoRA token and, per segment, one partial item
+    // beyond n / 4) must come to at most 3 per CTA: each costs the CTA's epilogue threads a round
+    // trip to memory, and more would keep the shrink running past the main loop.
+    const long long items = std::min(n, pv.S) + (n + 3) / 4;
+    const long long units = items * (pv.R / 8) * parts;
+    if (units > 3LL * p.m_tiles * p.splits) return 0;
+    // every CTA waits for the shrink shares of all the others: the whole grid must be resident
+    return p.m_tiles <= decode_max_clusters(p) ? 1 : 0;
+}
+
 template <typename T>
 static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
                        int s_parts, void* y, bool fuse, const void* prefetch, size_t prefetch_bytes,
-                       const GroupView* grp, cudaStream_t st) {
+                       const GroupView* grp, cudaStream_t st, bool grid_shrink) {
     using namespace tc;
     const int n = sv.n;
     if (n == 0) return LORA_OK;
@@ -1237,6 +1456,10 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.prefetch = static_cast<const char*>(prefetch);
         a.prefetch_bytes = prefetch ? prefetch_bytes : 0;
         a.stamp = take_kernel_stamp();
+        a.grid_shrink = grid_shrink && fuse && g1.count == 1 ? 1 : 0;
+        a.x = x;
+        a.s_out = const_cast<float*>(s_in);
+        a.ctr = const_cast<int*>(sv.nseg) + 2;
         static bool attr_set = false;
         if (!attr_set) {
             LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1354,10 +1577,12 @@ int launch_gemm_tall(const PoolView& pv, const SegView& sv, const void* W, const
 
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
                    void* y, bool fuse, cudaStream_t st, const void* prefetch, size_t prefetch_bytes,
-                   const GroupView* grp) {
+                   const GroupView* grp, bool grid_shrink) {
     if (pv.dtype == LORA_F16)
-        return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st);
-    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st);
+        return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st,
+                                   grid_shrink);
+    return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st,
+                                      grid_shrink);
 }
 
 }  // namespace lora

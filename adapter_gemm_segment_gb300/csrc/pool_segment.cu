@@ -180,6 +180,12 @@ segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restri
     constexpr int U = 4;  // tokens per thread whose loads are issued together
 
     pdl_wait();  // idx and the slot table may come from earlier kernels in the stream
+    // hand-off counters of the decode GEMMs that compute the shrink in their own grid (produced,
+    // consumed); each such GEMM leaves them at zero for the next linear over these segments
+    if (tid == 0) {
+        nseg_out[2] = 0;
+        nseg_out[3] = 0;
+    }
     for (int i = tid; i < K; i += kSegThreads) {
         cnt[i] = 0;
         const SlotEntry e = i > 0 ? table[i - 1] : SlotEntry{0, 0, 0.f, 0};

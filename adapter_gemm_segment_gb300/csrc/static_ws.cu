@@ -89,21 +89,7 @@ extern "C" int lora_linear_fwd_static_ws(lora_pool_t pool, const void* W_dev, co
     void* ws = nullptr;
     int rc = static_ws_address(pool->device, &ws);
     if (rc) return rc;
-    float* s_buf = static_cast<float*>(ws);
-    if (variant == LORA_VARIANT_AUTO) lora_linear_policy(pool, n, &variant);
-    const SegView sv = seg_view(seg);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool tc = variant != LORA_VARIANT_CUDA_CORE && tc_supported(pv, n);
-    const bool fused = variant != LORA_VARIANT_SEPARATE;
-    int s_parts = 1;
-    if (tc && n > 256 && shrink_tc_supported(pv))
-        rc = launch_shrink_tc(pv, sv, x_dev, s_buf, st);
-    else
-        rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256, &s_parts);
-    if (rc) return rc;
-    rc = tc ? launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st)
-            : launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
-    if (rc) return rc;
-    if (!fused) return launch_expand(pv, sv, s_buf, s_parts, y_dev, st);
-    return LORA_OK;
+    // the same launch sequence as lora_linear_fwd, with the library's array as the workspace
+    return linear_fwd_impl(pool, W_dev, x_dev, y_dev, seg, variant, static_cast<float*>(ws), nullptr, 0,
+                           static_cast<cudaStream_t>(stream));
 }

@@ -72,6 +72,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Load with acquire semantics at GPU scope (a flag another CTA released).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // A pipeline wait gave up: record it in the batch's status word (output of this call invalid).
 __device__ __forceinline__ void report_timeout_status(int32_t* status) { atomicExch(status, -9 /* LORA_ETIMEOUT */); }
 

@@ -345,6 +345,50 @@ def test_repeated_calls_are_bit_identical(lib):
         assert torch.equal(y, ys[0])
 
 
+@pytest.mark.parametrize("n", [1, 8])
+def test_fused_decode_computes_the_shrink_in_its_own_grid(lib, n):
+    """A fused decode linear of up to 8 tokens whose GEMM grid fits on the GPU at once launches
+    one kernel: the shrink runs inside the GEMM's grid.  Linears over one segment table on one
+    stream hand the shrink output over through counters in the segment workspace, which every
+    such linear leaves at zero: a chain of them, and a chain after a rebuilt segment table,
+    stays exact."""
+    case = wl.decode_q_proj(n=n, h=4096)
+    pool = make_pool(lib, case)
+    W, x = case.W.to(DEV), case.x.to(DEV)
+    ref = O.lora_linear_case(case)
+    seg = pool.segment(case.idx.to(DEV))
+    torch.cuda.synchronize()
+    c0 = lib.lora_kernel_launch_count()
+    y = pool.linear(W, x, seg, variant=1)
+    assert lib.lora_kernel_launch_count() - c0 == 1
+    ys = [pool.linear(W, x, seg, variant=1) for _ in range(6)]
+    seg2 = pool.segment(case.idx.to(DEV))
+    ys += [pool.linear(W, x, seg2, variant=1) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert_parity(y.cpu(), ref, "in-grid shrink")
+    for k, yk in enumerate(ys):
+        assert torch.equal(yk, y), f"linear {k} of the chain differs"
+    nseg = lib.segment_arrays(seg2)["nseg"].cpu().tolist()
+    assert nseg[2] == 0 and nseg[3] == 0, f"hand-off counters left at {nseg[2:]}"
+
+
+@pytest.mark.parametrize("n,h_out", [(16, 4096), (48, 10240)])
+def test_fused_decode_with_the_shrink_kernel(lib, n, h_out):
+    """Batches above 8 tokens keep the separate shrink kernel before the fused GEMM."""
+    case = wl.random_case(72, n, 256, h_out, [8, 16, 8], r_max=16, dtype=torch.bfloat16)
+    pool = make_pool(lib, case)
+    seg = pool.segment(case.idx.to(DEV))
+    torch.cuda.synchronize()
+    c0 = lib.lora_kernel_launch_count()
+    y = pool.linear(case.W.to(DEV), case.x.to(DEV), seg, variant=1)
+    assert lib.lora_kernel_launch_count() - c0 == 2
+    torch.cuda.synchronize()
+    assert_parity(y.cpu(), O.lora_linear_case(case), "fused decode after the shrink kernel")
+    y0 = pool.linear(torch.zeros_like(case.W).to(DEV), case.x.to(DEV), seg, variant=1).cpu()
+    assert_lora_only_parity(y0, O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case),
+                                              case.idx.numpy()), "fused decode after the shrink kernel, W=0")
+
+
 # ------------------------------------------------------------------------------------------
 # the five workloads
 # ------------------------------------------------------------------------------------------
