@@ -345,6 +345,20 @@ def test_repeated_calls_are_bit_identical(lib):
         assert torch.equal(y, ys[0])
 
 
+def test_variant_policy_follows_the_measured_sweep(lib):
+    """LORA_VARIANT_AUTO against the fused-vs-separate sweep on GB300 (4096 x 4096 fp16):
+    r_max 8 with 100 adapters fused up to 128 tokens, separate at 192 and 256; r_max 64 on 6
+    adapters fused up to 96 tokens, separate at 128 and 256."""
+    dec = lib.LoraPool(4096, 4096, 8, 100, torch.float16, DEV)  # empty slots count at r_max 8
+    mix = make_pool(lib, wl.mixed_rank(8))  # ranks {8, 8, 16, 16, 64, 64} mounted, as in the sweep
+    F, S = lib.LORA_VARIANT_FUSED, lib.LORA_VARIANT_SEPARATE
+    for n, want in ((1, F), (8, F), (64, F), (96, F), (128, F), (192, S), (256, S)):
+        assert lib.lora_linear_policy(dec.handle, n) == want, f"r_max 8, {n} tokens"
+    for n, want in ((1, F), (64, F), (96, F), (128, S), (256, S)):
+        assert lib.lora_linear_policy(mix.handle, n) == want, f"r_max 64, {n} tokens"
+    assert lib.lora_linear_policy(dec.handle, 4096) == F  # prefill batches are fused
+
+
 @pytest.mark.parametrize("n", [1, 8])
 def test_fused_decode_computes_the_shrink_in_its_own_grid(lib, n):
     """A fused decode linear of up to 8 tokens whose GEMM grid fits on the GPU at once launches
