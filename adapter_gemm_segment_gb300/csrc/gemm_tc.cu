@@ -1109,278 +1109,6 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 }
 
 // ============================================================================================
-// prefill on CTA pairs: persistent 256 x 256 tiles, one per cluster of two CTAs (cta_group::2)
-// ============================================================================================
-// A pair computes a tile of 256 tokens x 256 features.  For each 64-wide K step CTA r stages the
-// tile's x rows 128r .. 128r+127 and its W rows (features) 128r .. 128r+127; the even CTA's MMA
-// thread issues M = 256 x N = 256 pair MMAs that read both CTAs' halves, and each CTA's tensor
-// memory receives its 128 tokens x 256 features, which its own epilogue drains exactly as the
-// one-CTA kernel does.  Per CTA and K step that is 32 KB of operands for 128 x 256 outputs,
-// against 48 KB in the one-CTA kernel, whose main loop is limited by that operand delivery into
-// shared memory.
-// The odd CTA's copies complete on the even CTA's full barrier (the cta_group::2 form of the
-// tensor copy), which expects the bytes of both halves.  Stage and accumulator releases come
-// back by the MMA commits' multicast to both CTAs; the odd CTA's epilogue warps arrive on the
-// even CTA's acc_empty remotely.  Every wait is bounded, and both CTAs always reach the closing
-// cluster barrier.  (A first version relayed the odd CTA's readiness through its own barrier
-// and a remote arrive per stage: 1.8 ms per grouped 16384-token launch with a release fence in
-// each arrive, 0.96 ms without, against 0.80 ms for the one-CTA kernel.)
-constexpr int kPairBM = 2 * BM;  // tokens per pair tile
-constexpr bool kPrefillPairs = false;  // measured slower than the one-CTA kernel (see below)
-
-__device__ __forceinline__ void prefill_pair_tile(int tile, int m_tiles, int n_tiles, int& m0, int& n0) {
-    const int per_group = m_tiles * kPrefillNGroup;
-    const int g = tile / per_group;
-    const int gw = min(kPrefillNGroup, n_tiles - g * kPrefillNGroup);
-    const int r = tile - g * per_group;
-    m0 = (r / gw) * kPairBM;
-    n0 = (g * kPrefillNGroup + r % gw) * kPrefillBN;
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_prefill_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                         const PrefillArgs a) {
-    constexpr int BN = kPrefillBN;  // features per pair tile
-    constexpr int HN = BN / 2;      // W rows staged by each CTA
-    stamp_start(a.stamp);
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_align(smem_raw, 1024);
-    const int stages = a.stages;
-    constexpr uint32_t x_bytes = BM * BK * 2;
-    constexpr uint32_t w_bytes = HN * BK * 2;
-    constexpr uint32_t stage_bytes = x_bytes + w_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);  // even CTA: both halves
-    uint64_t* empty = full + stages;      // arrived by the even CTA's MMA commits (multicast)
-    uint64_t* acc_full = empty + stages;  // [2] (multicast)
-    uint64_t* acc_empty = acc_full + 2;   // [2] even CTA: the 8 epilogue warps of the pair
-    uint64_t* drained = acc_empty + 2;    // even CTA: every MMA it issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 1);
-    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int total = a.m_tiles * a.n_tiles;  // pair tiles; m_tiles counts 256-token tiles
-    const int nkb = a.kb_total;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 8);  // 4 epilogue warps in each CTA of the pair
-        }
-        mbar_init(drained, 1);
-        flags[0] = 0;
-        fence_barrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmX);
-        prefetch_tmap(&tmW);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(tmem_slot, 2 * BN);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();  // both CTAs' barriers exist before either CTA arrives on the other's
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    pdl_trigger();
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // Both CTAs' copies of a stage complete on the even CTA's full barrier, which expects
-            // the bytes of both halves; the odd CTA names that barrier by its cluster address.
-            const uint32_t full0 = mapa_shared(smem_u32(full), 0);
-            auto load = [&](int s, const CUtensorMap* m, uint32_t off, int c0, int c1) {
-                if (rank == 0)
-                    tma_load_2d(smem + s * stage_bytes + off, m, &full[s], c0, c1);
-                else
-                    tma_load_2d_pair(smem + s * stage_bytes + off, m, full0 + static_cast<uint32_t>(s) * 8u, c0, c1);
-            };
-            int it = 0;
-            bool waited = false;
-            int deferred = 0;
-            int def_kb[16], def_m[16];
-            for (int tile = pair; tile < total && !flags[0]; tile += npairs) {
-                int m0, n0;
-                prefill_pair_tile(tile, a.m_tiles, a.n_tiles, m0, n0);
-                const int xm = m0 + static_cast<int>(rank) * BM, wn = n0 + static_cast<int>(rank) * HN;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % stages;
-                    const uint32_t ph = (it / stages) & 1;
-                    if (it >= stages && !mbar_wait(&empty[s], ph ^ 1, flags)) break;
-                    if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * stage_bytes);
-                    load(s, &tmW, x_bytes, kb * BK, wn);
-                    if (waited) {
-                        load(s, &tmX, 0, kb * BK, xm);
-                    } else {
-                        // first ring pass: weights first, x after the previous grid finished
-                        def_kb[deferred] = kb;
-                        def_m[deferred] = xm;
-                        ++deferred;
-                        if (deferred == stages) {
-                            pdl_wait();
-                            waited = true;
-                            for (int d = 0; d < deferred; ++d) load(d, &tmX, 0, def_kb[d] * BK, def_m[d]);
-                        }
-                    }
-                }
-            }
-            if (!waited) {
-                pdl_wait();
-                for (int d = 0; d < deferred; ++d) load(d, &tmX, 0, def_kb[d] * BK, def_m[d]);
-            }
-            // aborted: the even CTA lets every copy in flight (its own and its pair's, counted on
-            // its barriers) land before the pair's closing barrier lets either CTA leave
-            if (flags[0] && rank == 0) {
-                report_timeout_status(a.seg.status);
-                for (int i = max(0, it - stages); i < it; ++i) {
-                    const unsigned long long t0 = globaltimer();
-                    while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // MMA thread of the pair
-            const uint32_t idesc = idesc_f16(kPairBM, BN, a.bf16 != 0);
-            int it = 0, local = 0;
-            bool ok = true;
-            for (int tile = pair; tile < total && ok; tile += npairs, ++local) {
-                const int buf = local & 1;
-                const uint32_t acc = tmem + buf * BN;
-                if (!mbar_wait(&acc_empty[buf], ((local >> 1) & 1) ^ 1, flags)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % stages;
-                    const uint32_t ph = (it / stages) & 1;
-                    if (!mbar_wait(&full[s], ph, flags)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t xa = smem_u32(smem + s * stage_bytes);
-                    const uint32_t wa = xa + x_bytes;
-#pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k)
-                        umma_pair_f16(acc, sdesc_sw128(xa + k * UMMA_K * 2), sdesc_sw128(wa + k * UMMA_K * 2), idesc,
-                                      (kb > 0 || k > 0) ? 1u : 0u);
-                    umma_pair_commit_multicast(&empty[s], 0x3);
-                }
-                if (!ok) break;
-                umma_pair_commit_multicast(&acc_full[buf], 0x3);
-            }
-            if (!ok) report_timeout_status(a.seg.status);
-            // every MMA issued above has completed before the pair may tear down
-            umma_pair_commit_multicast(drained, 0x1);
-            const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait(drained, 0) && globaltimer() - t0 < kWaitLimitNs) {
-            }
-        }
-    } else {
-        // ---- epilogue: thread <-> token row (TMEM lane) of this CTA's half, 256 features ----
-        const int q = warp & 3;
-        const int ldy = a.grp.ldy, R = a.pool.R, n = a.n;
-        T* y = static_cast<T*>(a.y);
-        bool waited = false;
-        int status = LORA_OK;
-        int local = 0;
-        const uint32_t peer_acc_empty = mapa_shared(smem_u32(acc_empty), 0);
-        for (int tile = pair; tile < total; tile += npairs, ++local) {
-            const int buf = local & 1;
-            const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (local >> 1) & 1, flags));
-            if (!got) break;
-            tc_fence_after();
-            if (!waited) {
-                pdl_wait();
-                status = __ldcg(a.seg.status);
-                waited = true;
-            }
-            int m0, n0;
-            prefill_pair_tile(tile, a.m_tiles, a.n_tiles, m0, n0);
-            const int t = m0 + static_cast<int>(rank) * BM + q * 32 + lane;
-            const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
-            const int slot = (a.fuse && t < n) ? __ldcg(a.seg.idx + t) : -1;
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-                uint32_t r[16];
-                __syncwarp();
-                tmem_ld16(taddr + c0, r);
-                tmem_ld_wait();
-                const int col = n0 + c0;  // column of y
-                if (status != LORA_OK || t >= n || col >= ldy) continue;  // after the warp-wide load
-                float v[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
-                if (slot >= 0) {
-                    // the slice owning these 16 columns (slice boundaries are multiples of 16)
-                    const SliceRef sl = group_slice(a.grp, group_slice_of_col(a.grp, col));
-                    const float* srow = a.s_in + sl.s_off + (size_t)t * R;
-                    const T* Bt = static_cast<const T*>(sl.B) + ((size_t)slot * sl.h_out + (col - sl.col)) * R;
-                    const int cmax = min(16, sl.col + sl.h_out - col);
-                    for (int j0 = 0; j0 < R; j0 += 8) {
-                        const float4 sa = __ldg(reinterpret_cast<const float4*>(srow + j0));
-                        const float4 sb = __ldg(reinterpret_cast<const float4*>(srow + j0 + 4));
-                        uint4 bv[16];
-#pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            bv[c] = c < cmax ? __ldg(reinterpret_cast<const uint4*>(Bt + (size_t)c * R + j0))
-                                             : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            float b[8];
-                            unpack8<T>(bv[c], b);
-                            float acc = v[c];
-                            acc = fmaf(b[0], sa.x, acc);
-                            acc = fmaf(b[1], sa.y, acc);
-                            acc = fmaf(b[2], sa.z, acc);
-                            acc = fmaf(b[3], sa.w, acc);
-                            acc = fmaf(b[4], sb.x, acc);
-                            acc = fmaf(b[5], sb.y, acc);
-                            acc = fmaf(b[6], sb.z, acc);
-                            acc = fmaf(b[7], sb.w, acc);
-                            v[c] = acc;
-                        }
-                    }
-                }
-                T* yp = y + (size_t)t * ldy + col;
-                alignas(16) T outv[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) outv[c] = from_f32<T>(v[c]);
-                if (col + 16 <= ldy) {
-                    reinterpret_cast<uint4*>(yp)[0] = reinterpret_cast<const uint4*>(outv)[0];
-                    reinterpret_cast<uint4*>(yp)[1] = reinterpret_cast<const uint4*>(outv)[1];
-                } else {  // h_out is a multiple of 8: one half-chunk remains
-                    reinterpret_cast<uint4*>(yp)[0] = reinterpret_cast<const uint4*>(outv)[0];
-                }
-            }
-            tc_fence_before();
-            if (lane == 0) {
-                if (rank == 0)
-                    mbar_arrive(&acc_empty[buf]);
-                else
-                    mbar_arrive_remote(peer_acc_empty + static_cast<uint32_t>(buf) * 8u);
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();  // neither CTA leaves (or frees tensor memory) while its pair may still use it
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc_pair(tmem, 2 * BN);
-    stamp_end(a.stamp);
-}
-
-// ============================================================================================
 // tall-tile base GEMM (no LoRA term) for grouped batches of 128-256 tokens
 // ============================================================================================
 // At 128-256 tokens the x tile of a stage is as large as the W tile or larger, and every row
@@ -1787,65 +1515,6 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     CUtensorMap mX, mW;
     int rc = make_map(&mX, x, bf16, pv.h_in, n, BM);
     if (rc) return rc;
-    if (kPrefillPairs && num_sms() >= 2) {
-        // CTA pairs: 256-token x 256-feature tiles, each CTA staging 128 rows of x and of W
-        a.m_tiles = (n + kPairBM - 1) / kPairBM;
-        const int pstage = (BM + kPrefillBN / 2) * BK * 2;
-        a.stages = std::min(6, kSmemBudget / pstage);
-        rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, kPrefillBN / 2);
-        if (rc) return rc;
-        const size_t psmem = (size_t)a.stages * pstage + 1024 + 256;
-        static bool pattr = false;
-        if (!pattr) {
-            LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_prefill_pair_kernel<T>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 8 * 1024));
-            pattr = true;
-        }
-        // a persistent grid: only as many pairs as the GPU holds at once (an SM left over in a
-        // GPC with an odd number of free SMs cannot host a pair), or the last pairs would run as
-        // a second wave
-        static int max_pairs = 0;
-        if (!max_pairs) {
-            cudaLaunchConfig_t q;
-            memset(&q, 0, sizeof(q));
-            q.gridDim = dim3(2 * (num_sms() / 2));
-            q.blockDim = dim3(kThreads);
-            q.dynamicSmemBytes = psmem;
-            cudaLaunchAttribute qa[1];
-            qa[0].id = cudaLaunchAttributeClusterDimension;
-            qa[0].val.clusterDim.x = 2;
-            qa[0].val.clusterDim.y = 1;
-            qa[0].val.clusterDim.z = 1;
-            q.attrs = qa;
-            q.numAttrs = 1;
-            int c = 0;
-            if (cudaOccupancyMaxActiveClusters(&c, (const void*)gemm_prefill_pair_kernel<T>, &q) != cudaSuccess || c < 1) {
-                (void)cudaGetLastError();
-                c = num_sms() / 2;
-            }
-            max_pairs = std::min(c, num_sms() / 2);
-        }
-        const int pairs = std::min(a.m_tiles * a.n_tiles, max_pairs);
-        void* args[] = {(void*)&mX, (void*)&mW, (void*)&a};
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof(cfg));
-        cfg.gridDim = dim3(2 * pairs);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = psmem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[2];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 2;
-        LORA_CUDA_TRY(cudaLaunchKernelExC(&cfg, (const void*)gemm_prefill_pair_kernel<T>, args));
-        count_launch();
-        return LORA_OK;
-    }
     rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, kPrefillBN);
     if (rc) return rc;
     const size_t smem = (size_t)a.stages * stage_bytes + 1024 + 256;

@@ -118,17 +118,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
-// 2-D tiled load into this CTA's shared memory whose completion (bytes) is counted on an
-// mbarrier of the even CTA of this CTA's pair (bar_cluster_addr from mapa_shared): the odd CTA
-// of a cta_group::2 pipeline fills its half of a stage and the even CTA's barrier sees it land.
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster_addr, int c0,
-                                                 int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
-        "%3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar_cluster_addr)
-        : "memory");
-}
 // 2-D tiled store of a shared-memory box to global memory (elements outside the tensor are
 // skipped); tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int c0, int c1) {
@@ -247,47 +236,7 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// ---- tcgen05 on a CTA pair (cta_group::2) -----------------------------------------------------------
-// Tensor memory of a CTA pair: one warp of each of the two CTAs allocates together, and both
-// get the same column address; the same holds for relinquish and dealloc.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// D[tmem of both CTAs] (+)= A * B^T over the pair, issued by one thread of the even CTA: A's M
-// rows come half from each CTA's shared memory and B's N rows half from each, at the same
-// shared-memory addresses; each CTA's tensor memory receives its half of D's rows.
-__device__ __forceinline__ void umma_pair_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive (once) on the mbarrier at `bar`'s offset in every CTA of cta_mask when the pair MMAs
-// issued so far by this thread have completed.
-__device__ __forceinline__ void umma_pair_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // ---- thread-block clusters / distributed shared memory ---------------------------------------
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared), releasing this
-// thread's earlier memory operations at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
