@@ -343,6 +343,10 @@ int lora_linear_fwd_group(int count, const lora_pool_t* pools, const void* W_dev
     pcat.h_out = grp.ldy;
     if (!tc_supported(pcat, n)) return set_error(LORA_EUNSUP, "no tensor-core plan for this group and batch");
     if (variant == LORA_VARIANT_AUTO) lora_linear_group_policy(count, pools, n, &variant);
+    if (count == 1)  // one slice: exactly the single linear's launch sequence
+        return linear_fwd_impl(pools[0], W_dev, x_dev, y_dev, seg, variant,
+                               reinterpret_cast<float*>(static_cast<char*>(ws_dev) + lin_layout(p0, n).s_off), nullptr, 0,
+                               static_cast<cudaStream_t>(stream));
     const bool fused = variant == LORA_VARIANT_FUSED;
     const bool decode = n <= 256;
     if (decode && fused)

@@ -627,7 +627,7 @@ def test_group_parity(lib, spec, variant):
 
 
 @pytest.mark.parametrize("variant", [1, 2])
-@pytest.mark.parametrize("n", [16, 64, 300])
+@pytest.mark.parametrize("n", [1, 8, 16, 64, 300])
 def test_group_of_one_is_the_single_linear(lib, n, variant):
     case = wl.random_case(60, n, 512, 384, [8, 16, 8], r_max=16, dtype=torch.bfloat16)
     y1, pools, seg = run_group(lib, [case], variant)
