@@ -83,6 +83,7 @@ struct PrefillArgs {
     const float* s_in;
     void* y;
     int n, m_tiles, n_tiles, kb_total, stages, fuse, bf16;
+    int lora_mma;  // one more pipeline block per tile: the LoRA expand on the tensor core
     unsigned long long* stamp;  // benchmark instrumentation (nullptr: off)
 };
 
@@ -122,6 +123,14 @@ __device__ __forceinline__ float lora_term(const T* __restrict__ Brow, const flo
         acc = fmaf(b[7], s1.w, acc);
     }
     return acc;
+}
+
+// Eight float32 values rounded to the 16-bit type, as one 16-byte chunk.
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float4& lo, const float4& hi) {
+    alignas(16) T v[8] = {from_f32<T>(lo.x), from_f32<T>(lo.y), from_f32<T>(lo.z), from_f32<T>(lo.w),
+                          from_f32<T>(hi.x), from_f32<T>(hi.y), from_f32<T>(hi.z), from_f32<T>(hi.w)};
+    return *reinterpret_cast<const uint4*>(v);
 }
 
 // dot(B row of one feature, s row of one token) over r_max, both in shared memory.  Lanes walk
@@ -897,6 +906,16 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 // ============================================================================================
 // prefill: persistent 128 x 256 tiles, double-buffered accumulators
 // ============================================================================================
+// The LoRA expand of a tile runs on the tensor core as one more K block of its accumulator:
+// with the tile's distinct adapters d = 0..D-1 (D * r_max <= 64), the block's operands are
+//   A'[token, d * r_max + j] = s[token, j] if the token's adapter is d, else 0   (128 x 64)
+//   B'[col,   d * r_max + j] = B_d[col, j]                                      (256 x 64)
+// so that A' B'^T adds sum_j s[t, j] B_slot(t)[col, j] to every (token, column) of the tile
+// (s rounded to the 16-bit type, float32 accumulation).  The epilogue warps write both operands
+// into the pipeline stage that the block occupies, in the layout a 128-byte-swizzled TMA copy
+// would leave (16-byte chunk c of row r at chunk position c ^ (r % 8)), and complete the
+// stage's full barrier themselves; the producer skips that position.  Tiles with more
+// adapters, or whose columns span two slices of a group, keep the epilogue's SIMT expand.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -913,8 +932,9 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint64_t* empty = full + stages;
     uint64_t* acc_full = empty + stages;  // [2]
     uint64_t* acc_empty = acc_full + 2;   // [2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint64_t* lora_free = acc_empty + 2;  // the LoRA block's stage is free (one phase per tile)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lora_free + 1);
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [16]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = a.m_tiles * a.n_tiles;
@@ -929,6 +949,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
         }
+        mbar_init(lora_free, 1);
         flags[0] = 0;
         fence_barrier_init();
     }
@@ -946,45 +967,53 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     const uint32_t tmem = *tmem_slot;
     pdl_trigger();
 
+    // pipeline positions of a tile: its nkb K blocks, then (lora_mma) the LoRA block
+    const int per_tile = nkb + (a.lora_mma ? 1 : 0);
+
     if (warp == 0) {
         if (lane == 0) {
             int it = 0;
             bool waited = false;
             int deferred = 0;
-            int def_kb[16], def_m[16];
+            int def_kb[16], def_m[16], def_s[16];
+            // first ring pass: weights first, x after the previous grid finished
+            auto flush = [&]() {
+                pdl_wait();
+                waited = true;
+                for (int d = 0; d < deferred; ++d)
+                    tma_load_2d(smem + def_s[d] * stage_bytes, &tmX, &full[def_s[d]], def_kb[d] * BK, def_m[d]);
+            };
             for (int tile = blockIdx.x; tile < total && !flags[0]; tile += gridDim.x) {
                 int m0, n0;
                 prefill_tile(tile, a.m_tiles, a.n_tiles, m0, n0);
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = 0; kb < per_tile; ++kb, ++it) {
                     const int s = it % stages;
                     const uint32_t ph = (it / stages) & 1;
-                    if (it >= stages && !mbar_wait(&empty[s], ph ^ 1, flags)) break;
+                    if (it >= stages) {
+                        if (!waited) flush();
+                        if (!mbar_wait(&empty[s], ph ^ 1, flags)) break;
+                    }
+                    if (kb == nkb) {  // the LoRA block: its stage goes to the epilogue warps
+                        mbar_arrive(lora_free);
+                        continue;
+                    }
                     mbar_arrive_expect_tx(&full[s], stage_bytes);
                     tma_load_2d(smem + s * stage_bytes + x_bytes, &tmW, &full[s], kb * BK, n0);
                     if (waited) {
                         tma_load_2d(smem + s * stage_bytes, &tmX, &full[s], kb * BK, m0);
                     } else {
-                        // first ring pass: weights first, x after the previous grid finished
                         def_kb[deferred] = kb;
                         def_m[deferred] = m0;
+                        def_s[deferred] = s;
                         ++deferred;
-                        if (deferred == stages) {
-                            pdl_wait();
-                            waited = true;
-                            for (int d = 0; d < deferred; ++d)
-                                tma_load_2d(smem + d * stage_bytes, &tmX, &full[d], def_kb[d] * BK, def_m[d]);
-                        }
                     }
                 }
             }
-            if (!waited) {
-                pdl_wait();
-                for (int d = 0; d < deferred; ++d)
-                    tma_load_2d(smem + d * stage_bytes, &tmX, &full[d], def_kb[d] * BK, def_m[d]);
-            }
+            if (!waited) flush();
             if (flags[0]) {
                 report_timeout_status(a.seg.status);
                 for (int i = max(0, it - stages); i < it; ++i) {
+                    if (i % per_tile == nkb) continue;  // not a copy of this thread
                     const unsigned long long t0 = globaltimer();
                     while (!mbar_try_wait(&full[i % stages], (i / stages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
                     }
@@ -1004,7 +1033,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     break;
                 }
                 tc_fence_after();
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = 0; kb < per_tile; ++kb, ++it) {
                     const int s = it % stages;
                     if (!mbar_wait(&full[s], (it / stages) & 1, flags)) {
                         ok = false;
@@ -1013,10 +1042,16 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     tc_fence_after();
                     const uint32_t xa = smem_u32(smem + s * stage_bytes);
                     const uint32_t wa = xa + x_bytes;
+                    if (kb < nkb) {
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k)
-                        umma_f16(acc, sdesc_sw128(xa + k * UMMA_K * 2), sdesc_sw128(wa + k * UMMA_K * 2), idesc,
-                                 (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_f16(acc, sdesc_sw128(xa + k * UMMA_K * 2), sdesc_sw128(wa + k * UMMA_K * 2), idesc,
+                                     (kb > 0 || k > 0) ? 1u : 0u);
+                    } else {  // the LoRA block: K of its operands set by the epilogue warps (0: none)
+                        const int lk = flags[1];
+                        for (int k = 0; k < lk / UMMA_K; ++k)
+                            umma_f16(acc, sdesc_sw128(xa + k * UMMA_K * 2), sdesc_sw128(wa + k * UMMA_K * 2), idesc, 1u);
+                    }
                     umma_commit(&empty[s]);
                 }
                 umma_commit(&acc_full[buf]);
@@ -1031,21 +1066,98 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         bool waited = false;
         int status = LORA_OK;
         int local = 0;
+        const int et = threadIdx.x - 64;  // 0..127
+        volatile int* red = flags + 2;   // [4]: per-warp minima
+        volatile int* dsl = flags + 8;   // [8]: the tile's distinct adapters
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
             const int buf = local & 1;
-            const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (local >> 1) & 1, flags));
-            if (!got) break;
-            tc_fence_after();
             if (!waited) {
-                pdl_wait();
+                pdl_wait();  // s, idx and the status word come from earlier kernels
                 status = __ldcg(a.seg.status);
                 waited = true;
             }
             int m0, n0;
             prefill_tile(tile, a.m_tiles, a.n_tiles, m0, n0);
+            bool lora_done = false;  // the tile's LoRA term went through the tensor core
+            if (a.lora_mma) {
+                // ---- operands of the tile's LoRA block (token row et; columns et, et + 128) ----
+                const int tr = m0 + et;
+                const int slot_r = (status == LORA_OK && tr < n) ? __ldcg(a.seg.idx + tr) : -1;
+                const int qa = group_slice_of_col(a.grp, n0);
+                const int qb = group_slice_of_col(a.grp, min(n0 + BN, ldy) - 1);
+                const int dmax = 64 / R;
+                // distinct adapters of the tile in increasing order (uniform over the 128 threads)
+                int mine = -1, D = 0;
+                for (int d = 0; d <= dmax; ++d) {
+                    const int cand = __reduce_min_sync(0xffffffffu, (slot_r >= 0 && mine < 0) ? slot_r : INT_MAX);
+                    named_bar_sync(1, 128);  // the previous round has read red
+                    if (lane == 0) red[q] = cand;
+                    named_bar_sync(1, 128);
+                    const int m = min(min(red[0], red[1]), min(red[2], red[3]));
+                    if (m == INT_MAX) break;
+                    D = d + 1;
+                    if (d == dmax) break;  // more adapters than the block holds
+                    if (slot_r == m) mine = d;
+                    if (et == 0) dsl[d] = m;
+                }
+                const int lk = (D == 0 || D > dmax || qa != qb) ? 0 : (D * R + 15) / 16 * 16;
+                lora_done = lk > 0;
+                named_bar_sync(1, 128);  // dsl visible
+                uint4 av[8], bw[2][8];
+                if (lk > 0) {  // all loads first
+                    const SliceRef sl = group_slice(a.grp, qa);
+                    const float* srow = a.s_in + sl.s_off + (size_t)tr * R;
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const int d = c8 * 8 / R, j = c8 * 8 - d * R;
+                        av[c8] = make_uint4(0, 0, 0, 0);
+                        if (c8 * 8 < lk && d == mine)
+                            av[c8] = pack8<T>(__ldcg(reinterpret_cast<const float4*>(srow + j)),
+                                              __ldcg(reinterpret_cast<const float4*>(srow + j + 4)));
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int col = n0 + et + h * 128;
+                            bw[h][c8] = make_uint4(0, 0, 0, 0);
+                            if (c8 * 8 < lk && d < D && col < ldy)
+                                bw[h][c8] = __ldg(reinterpret_cast<const uint4*>(
+                                    static_cast<const T*>(sl.B) + ((size_t)dsl[d] * sl.h_out + (col - sl.col)) * R + j));
+                        }
+                    }
+                }
+                // the block's stage, once the producer has seen its previous use consumed (the
+                // producer walks the positions in order; one lora_free phase per tile)
+                const int s = (local * per_tile + nkb) % stages;
+                if (et == 0) mbar_wait(lora_free, local & 1, flags);
+                named_bar_sync(1, 128);
+                if (flags[0]) break;
+                if (lk > 0) {
+                    uint8_t* As = smem + s * stage_bytes;  // [128 token rows][128 B]
+                    uint8_t* Bs = As + x_bytes;            // [256 column rows][128 B]
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        if (c8 * 8 < lk) {
+                            *reinterpret_cast<uint4*>(As + et * 128 + ((c8 ^ (et & 7)) << 4)) = av[c8];
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int o = et + h * 128;
+                                *reinterpret_cast<uint4*>(Bs + o * 128 + ((c8 ^ (o & 7)) << 4)) = bw[h][c8];
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();  // read by the tensor core
+                }
+                named_bar_sync(1, 128);
+                if (et == 0) {
+                    flags[1] = lk;
+                    mbar_arrive(&full[s]);
+                }
+            }
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (local >> 1) & 1, flags));
+            if (!got) break;
+            tc_fence_after();
             const int t = m0 + q * 32 + lane;
             const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
-            const int slot = (a.fuse && t < n) ? __ldcg(a.seg.idx + t) : -1;
+            const int slot = (a.fuse && !lora_done && t < n) ? __ldcg(a.seg.idx + t) : -1;
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 uint32_t r[16];
                 __syncwarp();
@@ -1511,12 +1623,15 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     a.stages = std::min(4, kSmemBudget / stage_bytes);
     a.fuse = fuse ? 1 : 0;
     a.bf16 = bf16;
+    a.lora_mma = fuse && pv.R <= 64 ? 1 : 0;
     a.stamp = take_kernel_stamp();
     CUtensorMap mX, mW;
     int rc = make_map(&mX, x, bf16, pv.h_in, n, BM);
     if (rc) return rc;
     rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, kPrefillBN);
     if (rc) return rc;
+    // barriers (2 per stage, 4 accumulator, lora_free), the TMEM address and 16 flag words
+    if ((2 * a.stages + 5) * 8 + 4 + 16 * 4 > 256) return set_error(LORA_EINVAL, "internal: prefill barrier area");
     const size_t smem = (size_t)a.stages * stage_bytes + 1024 + 256;
     static bool attr = false;
     if (!attr) {

@@ -523,6 +523,35 @@ def test_prefill_grouped_tiles(lib, variant):
     _negative_control(y0[rows], group, pools_ref, rows=rows)
 
 
+# (seed, r_max, true ranks, run length, dtype): adapters in runs of `run length` tokens, every
+# seventh token base-only, so a 128-token tile holds the number of adapters noted
+PREFILL_BLOCK_CASES = [
+    (70, 8, [8] * 10, 16, torch.bfloat16),          # 8 per tile: the largest block at r_max 8
+    (71, 8, [8, 3] * 6, 13, torch.float16),         # 10-11 per tile: the epilogue's SIMT expand
+    (72, 16, [16, 5, 16, 9], 40, torch.bfloat16),   # 3-5 per tile (4 fit a block at r_max 16)
+    (73, 32, [32, 17, 32], 64, torch.float16),      # 2-3 per tile at r_max 32
+    (74, 64, [64, 33], 128, torch.bfloat16),        # one per tile
+    (75, 64, [64, 33, 50], 100, torch.float16),     # 1 or 2 per tile (SIMT when 2)
+]
+
+
+@pytest.mark.parametrize("seed,r_max,ranks,run_len,dtype", PREFILL_BLOCK_CASES)
+def test_prefill_lora_block_on_the_tensor_core(lib, seed, r_max, ranks, run_len, dtype):
+    """The prefill GEMM adds the LoRA term of a tile as one more tensor-core K block when the
+    tile's adapters fit it (count x r_max <= 64), else in its epilogue: tiles of both kinds
+    in one call, with base-only tokens, a ragged last token tile and a ragged column tile.
+    Every element against the oracle, and the LoRA term alone (W = 0)."""
+    n, S = 5 * 128 + 37, len(ranks)
+    idx = (np.arange(n) // run_len) % S
+    idx[::7] = -1
+    case = wl.random_case(seed, n, 256, 320, ranks, r_max=r_max, dtype=dtype, idx=idx)
+    y, pool, _ = run(lib, case, 1)
+    assert_parity(y, O.lora_linear_case(case), f"prefill LoRA block r_max {r_max} runs of {run_len}")
+    y0, _, _ = run(lib, case, 1, W=torch.zeros_like(case.W), pool=pool)
+    y0_ref = O.lora_linear(case.x, torch.zeros_like(case.W), O.pool_of_case(case), case.idx.numpy())
+    assert_lora_only_parity(y0, y0_ref, f"prefill LoRA block r_max {r_max} W=0")
+
+
 # ------------------------------------------------------------------------------------------
 # segments shared by pools whose slots hold different ranks
 # ------------------------------------------------------------------------------------------
