@@ -125,6 +125,20 @@ __device__ __forceinline__ float lora_term(const T* __restrict__ Brow, const flo
     return acc;
 }
 
+// Two float32 values rounded to the 16-bit type, packed (low half first).
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // Eight float32 values rounded to the 16-bit type, as one 16-byte chunk.
 template <typename T>
 __device__ __forceinline__ uint4 pack8(const float4& lo, const float4& hi) {
@@ -1158,56 +1172,57 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const int t = m0 + q * 32 + lane;
             const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
             const int slot = (a.fuse && !lora_done && t < n) ? __ldcg(a.seg.idx + t) : -1;
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-                uint32_t r[16];
+            // 32 columns per round: both TMEM loads, one wait, then two 16-column pieces
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
                 __syncwarp();
-                tmem_ld16(taddr + c0, r);
+                tmem_ld16(taddr + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+                tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
                 tmem_ld_wait();
-                const int col = n0 + c0;  // column of y
-                if (status != LORA_OK || t >= n || col >= ldy) continue;  // after the warp-wide load
-                float v[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
-                if (slot >= 0) {
-                    // the slice owning these 16 columns (slice boundaries are multiples of 16)
-                    const SliceRef sl = group_slice(a.grp, group_slice_of_col(a.grp, col));
-                    const float* srow = a.s_in + sl.s_off + (size_t)t * R;
-                    const T* Bt = static_cast<const T*>(sl.B) + ((size_t)slot * sl.h_out + (col - sl.col)) * R;
-                    const int cmax = min(16, sl.col + sl.h_out - col);
-                    for (int j0 = 0; j0 < R; j0 += 8) {
-                        const float4 sa = __ldg(reinterpret_cast<const float4*>(srow + j0));
-                        const float4 sb = __ldg(reinterpret_cast<const float4*>(srow + j0 + 4));
-                        uint4 bv[16];
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int col = n0 + c0 + 16 * hf;  // column of y
+                    if (status != LORA_OK || t >= n || col >= ldy) continue;  // after the warp-wide loads
+                    float v[16];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            bv[c] = c < cmax ? __ldg(reinterpret_cast<const uint4*>(Bt + (size_t)c * R + j0))
-                                             : make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[16 * hf + c]);
+                    if (slot >= 0) {
+                        // the slice owning these 16 columns (slice boundaries are multiples of 16)
+                        const SliceRef sl = group_slice(a.grp, group_slice_of_col(a.grp, col));
+                        const float* srow = a.s_in + sl.s_off + (size_t)t * R;
+                        const T* Bt = static_cast<const T*>(sl.B) + ((size_t)slot * sl.h_out + (col - sl.col)) * R;
+                        const int cmax = min(16, sl.col + sl.h_out - col);
+                        for (int j0 = 0; j0 < R; j0 += 8) {
+                            const float4 sa = __ldg(reinterpret_cast<const float4*>(srow + j0));
+                            const float4 sb = __ldg(reinterpret_cast<const float4*>(srow + j0 + 4));
+                            uint4 bv[16];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            float b[8];
-                            unpack8<T>(bv[c], b);
-                            float acc = v[c];
-                            acc = fmaf(b[0], sa.x, acc);
-                            acc = fmaf(b[1], sa.y, acc);
-                            acc = fmaf(b[2], sa.z, acc);
-                            acc = fmaf(b[3], sa.w, acc);
-                            acc = fmaf(b[4], sb.x, acc);
-                            acc = fmaf(b[5], sb.y, acc);
-                            acc = fmaf(b[6], sb.z, acc);
-                            acc = fmaf(b[7], sb.w, acc);
-                            v[c] = acc;
+                            for (int c = 0; c < 16; ++c)
+                                bv[c] = c < cmax ? __ldg(reinterpret_cast<const uint4*>(Bt + (size_t)c * R + j0))
+                                                 : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                float b[8];
+                                unpack8<T>(bv[c], b);
+                                float acc = v[c];
+                                acc = fmaf(b[0], sa.x, acc);
+                                acc = fmaf(b[1], sa.y, acc);
+                                acc = fmaf(b[2], sa.z, acc);
+                                acc = fmaf(b[3], sa.w, acc);
+                                acc = fmaf(b[4], sb.x, acc);
+                                acc = fmaf(b[5], sb.y, acc);
+                                acc = fmaf(b[6], sb.z, acc);
+                                acc = fmaf(b[7], sb.w, acc);
+                                v[c] = acc;
+                            }
                         }
                     }
-                }
-                T* yp = y + (size_t)t * ldy + col;
-                alignas(16) T outv[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) outv[c] = from_f32<T>(v[c]);
-                if (col + 16 <= ldy) {
-                    reinterpret_cast<uint4*>(yp)[0] = reinterpret_cast<const uint4*>(outv)[0];
-                    reinterpret_cast<uint4*>(yp)[1] = reinterpret_cast<const uint4*>(outv)[1];
-                } else {  // h_out is a multiple of 8: one half-chunk remains
-                    reinterpret_cast<uint4*>(yp)[0] = reinterpret_cast<const uint4*>(outv)[0];
+                    uint4* yp = reinterpret_cast<uint4*>(y + (size_t)t * ldy + col);
+                    yp[0] = make_uint4(pack2<T>(v[0], v[1]), pack2<T>(v[2], v[3]), pack2<T>(v[4], v[5]),
+                                       pack2<T>(v[6], v[7]));
+                    if (col + 16 <= ldy)  // else h_out (a multiple of 8) leaves one half-chunk
+                        yp[1] = make_uint4(pack2<T>(v[8], v[9]), pack2<T>(v[10], v[11]), pack2<T>(v[12], v[13]),
+                                           pack2<T>(v[14], v[15]));
                 }
             }
             tc_fence_before();
