@@ -56,6 +56,13 @@ struct PoolView {
 };
 
 // Segments as the kernels see them (device pointers).
+// Words of the segment workspace's nseg array after the segment and item counts: the
+// in-grid shrink's hand-off counters {produced, consumed}, then the x-ready word a decode
+// shrink publishes for the GEMM after it and the count of that GEMM's CTAs that have read it.
+constexpr int kGridShrinkWords = 2;
+constexpr int kXreadyWord = 4;
+constexpr int kXreadyCount = 5;
+
 struct SegView {
     const int32_t* perm;
     const int32_t* seg_start;
@@ -97,6 +104,10 @@ struct GroupView {
     long long s_stride;  // floats between the shrink outputs of consecutive slices
     int rank_aware;      // some mounted slot holds a rank below r_max: kernels may skip its padding
     unsigned long long* stamp;  // benchmark instrumentation of the launch (nullptr: off)
+    // Nonzero: the shrink kernel releases the fused decode GEMM after it at its start, and
+    // writes this value to the segments' x-ready word once its own dependency wait has
+    // returned (every kernel before it complete); the GEMM reads x after seeing that value.
+    int xready;
 };
 
 // Whether some slot of the pool (empty slots count at r_max) holds fewer 8-column chunks than
@@ -196,6 +207,10 @@ struct AuxStamp {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Store with release semantics at GPU scope (a flag other CTAs or grids acquire).
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }

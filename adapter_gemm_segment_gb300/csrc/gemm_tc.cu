@@ -74,6 +74,10 @@ struct DecodeArgs {
     const void* x;  // [n, h_in], read directly by the in-grid shrink
     float* s_out;
     int* ctr;
+    // x-ready hand-off with the shrink kernel before this grid (nonzero: the value it publishes
+    // in *xword once every earlier kernel is complete; xword[1] counts this grid's readers)
+    int xready;
+    int* xword;
 };
 
 struct PrefillArgs {
@@ -90,9 +94,11 @@ struct PrefillArgs {
 // Tile order of the persistent prefill kernel: output columns in groups of kPrefillNGroup
 // tiles (4096 features), and inside a group every token tile before the next group.  A wave of
 // CTAs then shares one group's weight (33.5 MB at 4096 inputs), which stays in L2 while the
-// token tiles stream past; x is read once per group.  Walking all column tiles of a wide
-// (concatenated q|v) weight in every wave instead evicted it: 1.6 GB of DRAM reads per 8192-wide
-// launch against 0.36 GB for its two 4096-wide halves.
+// token tiles stream past; x is read once per group.  Odd groups walk the token tiles in
+// reverse, so the first ones they need are the last the previous group read (still in L2).
+// Measured on GB300 (q|v as one 8192-wide launch, 16384 tokens bf16): DRAM reads 377 MB in
+// order, 367 MB snaking, same time; walking all 32 column tiles in every wave evicted the
+// weight (1.74 GB of reads, 5 % slower), also with evict-last hints on the weight's loads.
 constexpr int kPrefillNGroup = 16;
 
 __device__ __forceinline__ void prefill_tile(int tile, int m_tiles, int n_tiles, int& m0, int& n0) {
@@ -100,7 +106,7 @@ __device__ __forceinline__ void prefill_tile(int tile, int m_tiles, int n_tiles,
     const int g = tile / per_group;
     const int gw = min(kPrefillNGroup, n_tiles - g * kPrefillNGroup);  // column tiles in this group
     const int r = tile - g * per_group;
-    m0 = (r / gw) * BM;
+    m0 = ((g & 1) ? (m_tiles - 1 - r / gw) : (r / gw)) * BM;
     n0 = (g * kPrefillNGroup + r % gw) * kPrefillBN;
 }
 
@@ -396,7 +402,8 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     uint64_t* tmem_full = empty + stages;
     uint64_t* lbar = tmem_full + 1;  // LoRA operands staged
     uint64_t* rbar = lbar + 1;       // partial rows received
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 1);
+    uint64_t* xbar = rbar + 1;       // x-ready: the producer has seen the shrink's signal
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 1);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // abort, go, D, status, wsum[4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -441,9 +448,9 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     };
     // The producer thread initialises the barriers and fills the ring right away, so the first
     // HBM round trip overlaps the TMEM allocation and the CTA-wide barrier below.  With the
-    // in-grid shrink no kernel between the previous one and this grid has waited for it, so only
-    // the W boxes go out now (a weight is never written by the kernel just before the linear);
-    // the x boxes follow the grid-dependency wait.
+    // in-grid shrink or the x-ready hand-off, the previous linear may still be running, so only
+    // the W boxes go out now (a weight is never written by the kernels of the linear chain);
+    // the x boxes follow the grid-dependency wait or the hand-off.
     const int pre = min(stages, nkb);
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -453,12 +460,13 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         mbar_init(tmem_full, 1);
         mbar_init(lbar, 1);
         mbar_init(rbar, 1);
+        mbar_init(xbar, 1);
         for (int i = 0; i < 8; ++i) flags[i] = 0;
         fence_barrier_init();
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
         for (int i = 0; i < pre; ++i) {
-            if (a.grid_shrink)
+            if (a.grid_shrink || a.xready)
                 issue_w(i);
             else
                 issue_stage(i);
@@ -484,14 +492,41 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const T* B = static_cast<const T*>(a.pool.B);
 
     if (warp == 0) {
-        // W and x are complete when this grid starts if a shrink kernel precedes it in the
-        // stream: it releases its dependents only after its own grid-dependency wait, and only
-        // the shrink output (read by the epilogue warps) needs this grid's wait.  With the
-        // in-grid shrink this grid follows the previous kernel directly and waits itself before
-        // the first x box.
+        // Without a hand-off, W and x are complete when this grid starts if a shrink kernel
+        // precedes it in the stream: it releases its dependents only after its own
+        // grid-dependency wait, and only the shrink output (read by the epilogue warps) needs
+        // this grid's wait.  With the in-grid shrink this grid follows the previous kernel
+        // directly and waits itself before the first x box; with the x-ready hand-off it reads
+        // x once the shrink has published the pair's value.
         if (lane == 0) {
             if (a.grid_shrink) {
                 pdl_wait();
+                for (int i = 0; i < pre; ++i) issue_x(i);
+            } else if (a.xready) {
+                // The shrink kernel before this grid released it at its start and publishes the
+                // value once every earlier kernel is complete: x may then be read (through TMA,
+                // after a proxy fence); the weight boxes are already on their way.  The last CTA
+                // to read the value clears the word for the next linear over these segments.
+                const unsigned long long t0w = globaltimer();
+                bool seen = true;
+                while (ld_acquire_gpu(a.xword) != a.xready) {
+                    if (globaltimer() - t0w > kWaitLimitNs) {
+                        seen = false;
+                        break;
+                    }
+                    __nanosleep(32);
+                }
+                if (seen) {
+                    if (atomicAdd(a.xword + 1, 1) == (int)(gridDim.x * gridDim.y) - 1) {
+                        atomicExch(a.xword, 0);
+                        atomicExch(a.xword + 1, 0);
+                    }
+                } else {  // y is not written; x is still loaded, so that every copy completes
+                    flags[0] = 1;
+                    report_timeout_status(a.seg.status);
+                }
+                fence_proxy_async_global();
+                mbar_arrive(xbar);  // the epilogue warps may read the segments
                 for (int i = 0; i < pre; ++i) issue_x(i);
             }
             int issued = pre;  // stages 0 .. pre-1 went out before the CTA-wide barrier
@@ -538,8 +573,16 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
     } else {
         // ---- phase A (overlaps the main loop): stage this CTA's LoRA operands ----
-        pdl_wait();  // s (or x for the in-grid shrink), idx and the status word come from earlier kernels
-        if (et == 0) flags[3] = __ldcg(a.seg.status);
+        // s (or x for the in-grid shrink), idx and the status word come from earlier kernels.
+        // With the x-ready hand-off every kernel before the shrink is complete once the producer
+        // has seen its signal: the segments are read then, and only s waits for this grid's
+        // dependency wait (below, after the B tiles are on their way).
+        if (a.xready) {
+            if (et == 0) mbar_wait(xbar, 0, flags);
+        } else {
+            pdl_wait();
+        }
+        if (et == 0) flags[3] = flags[0] ? LORA_ETIMEOUT : __ldcg(a.seg.status);
         named_bar_sync(1, 128);
         const int n_ctas = gridDim.x * gridDim.y;
         // In-grid shrink: every CTA computes its share of the shrink units, then counts itself
@@ -575,6 +618,9 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (et == 0) atomicAdd(&a.ctr[0], 1);
         };
         const bool lora = flags[3] == LORA_OK && a.fuse;
+        // With the x-ready hand-off, this grid completes only after the shrink before it (as
+        // every later kernel's dependency wait assumes): the LoRA path waits below, this one here.
+        if (!lora && a.xready) pdl_wait();
         if (!lora && a.grid_shrink) {
             produce(false);
             wait_produced();
@@ -641,10 +687,14 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     }
                     pre_sm[0] = ns;
                     // bulk copies of the owned tokens' shrink parts (unless the in-grid shrink
-                    // is still writing them), then one TMA box per staged slot and 8-column
-                    // chunk: [128 feature rows][8 columns] of B
-                    const uint32_t sb = (cnt > 0 && !a.grid_shrink) ? a.s_parts * s_bytes : 0;
-                    mbar_arrive_expect_tx(lbar, sb + static_cast<uint32_t>(off) * 16);
+                    // is still writing them, or they come after this grid's dependency wait),
+                    // then one TMA box per staged slot and 8-column chunk: [128 feature rows][8
+                    // columns] of B
+                    const uint32_t sb = (cnt > 0 && !a.grid_shrink && !a.xready) ? a.s_parts * s_bytes : 0;
+                    if (a.xready)
+                        mbar_expect_tx(lbar, static_cast<uint32_t>(off) * 16);  // s: arrival below
+                    else
+                        mbar_arrive_expect_tx(lbar, sb + static_cast<uint32_t>(off) * 16);
                     if (sb)
                         for (int k = 0; k < a.s_parts; ++k)
                             bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
@@ -658,8 +708,11 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint32_t b_bytes = static_cast<uint32_t>(rows_valid * R * 2);
                     const int ns = min(min(running, kMaxPre), a.bpre_bytes / (BM * R * 2));
                     pre_sm[0] = ns;
-                    const uint32_t sb = (cnt > 0 && !a.grid_shrink) ? a.s_parts * s_bytes : 0;
-                    mbar_arrive_expect_tx(lbar, sb + ns * b_bytes);
+                    const uint32_t sb = (cnt > 0 && !a.grid_shrink && !a.xready) ? a.s_parts * s_bytes : 0;
+                    if (a.xready)
+                        mbar_expect_tx(lbar, ns * b_bytes);  // s: arrival below
+                    else
+                        mbar_arrive_expect_tx(lbar, sb + ns * b_bytes);
                     if (sb)
                         for (int k = 0; k < a.s_parts; ++k)
                             bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
@@ -669,6 +722,16 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 }
             }
             named_bar_sync(1, 128);
+            if (a.xready) {  // the shrink output: after this grid's dependency wait
+                pdl_wait();
+                if (et == 0) {
+                    const uint32_t s_bytes = static_cast<uint32_t>(cnt * R * 4);
+                    mbar_arrive_expect_tx(lbar, cnt > 0 ? a.s_parts * s_bytes : 0);
+                    if (cnt > 0)
+                        for (int k = 0; k < a.s_parts; ++k)
+                            bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
+                }
+            }
             if (a.grid_shrink) {  // this CTA's shrink share; the owned tokens' parts once the grid is done
                 produce(true);
                 wait_produced();
@@ -1531,7 +1594,7 @@ int decode_grid_shrink_ok(const PoolView& pv, int n) {
 template <typename T>
 static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
                        int s_parts, void* y, bool fuse, const void* prefetch, size_t prefetch_bytes,
-                       const GroupView* grp, cudaStream_t st, bool grid_shrink) {
+                       const GroupView* grp, cudaStream_t st, bool grid_shrink, int xready) {
     using namespace tc;
     const int n = sv.n;
     if (n == 0) return LORA_OK;
@@ -1587,6 +1650,8 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.prefetch_bytes = prefetch ? prefetch_bytes : 0;
         a.stamp = take_kernel_stamp();
         a.grid_shrink = grid_shrink && fuse && g1.count == 1 ? 1 : 0;
+        a.xready = a.grid_shrink ? 0 : xready;
+        a.xword = const_cast<int*>(sv.nseg) + kXreadyWord;
         a.x = x;
         a.s_out = const_cast<float*>(s_in);
         a.ctr = const_cast<int*>(sv.nseg) + 2;
@@ -1710,12 +1775,12 @@ int launch_gemm_tall(const PoolView& pv, const SegView& sv, const void* W, const
 
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
                    void* y, bool fuse, cudaStream_t st, const void* prefetch, size_t prefetch_bytes,
-                   const GroupView* grp, bool grid_shrink) {
+                   const GroupView* grp, bool grid_shrink, int xready) {
     if (pv.dtype == LORA_F16)
         return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st,
-                                   grid_shrink);
+                                   grid_shrink, xready);
     return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st,
-                                      grid_shrink);
+                                      grid_shrink, xready);
 }
 
 }  // namespace lora

@@ -11,9 +11,14 @@ namespace lora {
 // CUDA-core shrink.  Small batches of 16-bit data: one CTA per (sorted token, 8 adapter rows,
 // 1024 input features), *s_parts = ceil(h_in / 1024).  tiled: one CTA per (segment, 64 tokens)
 // through shared memory, *s_parts = 1.  float32: one warp per (token, rows), *s_parts = 1.
+// xready: nonzero for the small-batch kernels ahead of a fused decode GEMM launched with the
+// same value (GroupView::xready).
 int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled,
-                  int* s_parts);
+                  int* s_parts, int xready = 0);
 int shrink_parts(const PoolView& pv, int n, bool tiled);
+// Whether the small-batch shrink of 16-bit data takes the segmented kernel (A rows read once per
+// work item) rather than the per-token one.
+int shrink_segmented(const PoolView& pv, int n);
 // The same for the slices of a group (16-bit data, not tiled): slice q's output starts at
 // s_out + q * grp.s_stride.  One launch covers every slice.
 int launch_shrink_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,
@@ -45,9 +50,12 @@ int tc_supported(const PoolView& pv, int n);
 // concatenated width; y has row stride grp->ldy.  The prefill kernel applies every slice's
 // LoRA term; the decode kernel takes one slice with fuse, or several without the LoRA term
 // (a single slice may also be a column range of a wider y: pv.h_out < grp->ldy).
+// xready: nonzero when the shrink kernel just before this fused decode GEMM was launched with
+// the same value: the GEMM then streams its weight from its start and reads x once the shrink
+// has published the value.
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
                    void* y, bool fuse, cudaStream_t st, const void* prefetch = nullptr, size_t prefetch_bytes = 0,
-                   const GroupView* grp = nullptr, bool grid_shrink = false);
+                   const GroupView* grp = nullptr, bool grid_shrink = false, int xready = 0);
 
 // The launch sequence of one LoRA-augmented linear (lora_linear_fwd and its variants), after the
 // caller's arguments were checked; s_buf receives the shrink output.

@@ -72,6 +72,24 @@ shrink_warp_kernel(PoolView pool, SegView seg, const T* __restrict__ x, float* _
     }
 }
 
+// Grid-dependency wait of the decode shrinks, and the release of the base GEMM that follows.
+// Without an x-ready value the dependents are released after the wait: the GEMM then knows
+// that every kernel before this one has completed (x, W) and waits separately for s.  With
+// one, they are released at once -- the GEMM starts streaming its weight while the previous
+// linear finishes -- and the first CTA publishes the value once the wait has returned (x and
+// the segments complete); the GEMM loads x after reading it and waits for s as before.
+__device__ __forceinline__ void shrink_dependency_wait(const GroupView& grp, const SegView& seg) {
+    if (grp.xready) {
+        pdl_trigger();
+        pdl_wait();
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+            st_release_gpu(const_cast<int32_t*>(seg.nseg) + kXreadyWord, grp.xready);
+    } else {
+        pdl_wait();
+        pdl_trigger();
+    }
+}
+
 // ---- shrink for small batches: one CTA per (token, 8 adapter rows, K-part) -------------------
 // 128 threads each own 8 consecutive input features of every 1024-feature sweep, so a sweep
 // reads 2 KB of x and 16 KB of A with all nine 16-byte loads of a thread in flight; the K-parts
@@ -84,12 +102,9 @@ template <typename T>
 __global__ void __launch_bounds__(128)
 shrink_token_kernel(PoolView pool, GroupView grp, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
     __shared__ float red[4][8];
-    // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
-    // every kernel before this one has completed (x, W) and waits separately for s.
     AuxStamp stamp(grp.stamp);
-    pdl_wait();
+    shrink_dependency_wait(grp, seg);
     stamp.waited();
-    pdl_trigger();
     const int t = blockIdx.x, ks = blockIdx.z;
     const int h = pool.h_in, R = pool.R, rg = R / 8;
     // grid rows: (slice of the group, 8-row group of r_max)
@@ -160,12 +175,9 @@ template <typename T>
 __global__ void __launch_bounds__(128, 4)
 shrink_seg_kernel(PoolView pool, GroupView grp, SegView seg, const T* __restrict__ x, float* __restrict__ s_out) {
     __shared__ float red[4][32];
-    // Release dependents only after this grid's own wait: a dependent base GEMM then knows that
-    // every kernel before this one has completed (x, W) and waits separately for s.
     AuxStamp stamp(grp.stamp);
-    pdl_wait();
+    shrink_dependency_wait(grp, seg);
     stamp.waited();
-    pdl_trigger();
     const int b = blockIdx.x, ks = blockIdx.z;
     const int h = pool.h_in, R = pool.R, rg = R / 8;
     // grid rows: (slice of the group, 8-row group of r_max)
@@ -566,12 +578,7 @@ static int launch_shrink_t(const PoolView& pv, const GroupView& grp, const SegVi
             g1.stamp = take_aux_stamp();
             void* args[] = {(void*)&pv, (void*)&g1, (void*)&sv, (void*)&xp, (void*)&s_out};
             const int rows = grp.count * (pv.R / 8);  // (slice, 8-row group) pairs
-            // Per token, every LoRA token re-reads its adapter's A rows: n * r_max * h_in * 2
-            // bytes at most.  Past 16 MB (r_max 64 at 64 tokens, 4096 features: 33.5 MB) the
-            // segmented kernel reads each adapter once per 4 tokens instead (GB300, 32 chained
-            // 4096x4096 linears: r_max 64, 64 tokens 9 % faster; r_max 8 9 % slower, since its
-            // CTAs then take up to 4 tokens each on the shrink's critical path).
-            if ((double)sv.n * pv.R * pv.h_in * 2 >= 16.0 * (1 << 20)) {
+            if (shrink_segmented(pv, sv.n)) {
                 // at most one item per LoRA token, and per segment one partial item beyond n / 4
                 const int items = std::min(sv.n, std::min(sv.n, pv.S) + (sv.n + kItemTok - 1) / kItemTok);
                 LORA_CUDA_TRY(launch_pdl((const void*)shrink_seg_kernel<T>, dim3(items, rows, *s_parts), dim3(128), 0,
@@ -608,9 +615,20 @@ static int launch_shrink_t(const PoolView& pv, const GroupView& grp, const SegVi
     return LORA_OK;
 }
 
+// Per token, every LoRA token re-reads its adapter's A rows: n * r_max * h_in * 2 bytes at
+// most.  Past 16 MB (r_max 64 at 64 tokens, 4096 features: 33.5 MB) the segmented kernel reads
+// each adapter once per 4 tokens instead (GB300, 32 chained 4096x4096 linears: r_max 64, 64
+// tokens 9 % faster; r_max 8 9 % slower, since its CTAs then take up to 4 tokens each on the
+// shrink's critical path).
+int shrink_segmented(const PoolView& pv, int n) {
+    return (double)n * pv.R * pv.h_in * 2 >= 16.0 * (1 << 20) ? 1 : 0;
+}
+
 int launch_shrink(const PoolView& pv, const SegView& sv, const void* x, float* s_out, cudaStream_t st, bool tiled,
-                  int* s_parts) {
-    return launch_shrink_group(pv, single_group(pv), sv, x, s_out, st, tiled, s_parts);
+                  int* s_parts, int xready) {
+    GroupView g = single_group(pv);
+    g.xready = xready;
+    return launch_shrink_group(pv, g, sv, x, s_out, st, tiled, s_parts);
 }
 
 int launch_shrink_group(const PoolView& pv, const GroupView& grp, const SegView& sv, const void* x, float* s_out,

@@ -403,6 +403,57 @@ def test_fused_decode_with_the_shrink_kernel(lib, n, h_out):
                                               case.idx.numpy()), "fused decode after the shrink kernel, W=0")
 
 
+@pytest.mark.parametrize("n", [16, 48])
+def test_chained_fused_decode_hands_x_over_from_the_shrink(lib, n):
+    """Fused decode GEMMs after the per-token shrink start streaming their weight while the
+    previous linear finishes and read x once the shrink has published a value unique to the
+    pair (the x-ready word of the segments).  A chain of linears over one set of segments,
+    each fed the previous output: every output against the oracle run on the GPU's own input,
+    the hand-off words cleared after the chain, and a graph replay of the chain (the same
+    values again) bit-identical to the eager run, twice."""
+    h, L = 512, 6
+    case = wl.random_case(73, n, h, h, [8, 16, 8, 4], r_max=16, dtype=torch.float16)
+    pool = make_pool(lib, case)
+    seg = pool.segment(case.idx.to(DEV))
+    rng = np.random.default_rng(74)
+    Ws = [torch.from_numpy(rng.standard_normal((h, h)) * 0.05).to(torch.float16).to(DEV) for _ in range(L)]
+    ys = [torch.empty(n, h, dtype=torch.float16, device=DEV) for _ in range(L)]
+    ws = torch.empty(lib.lora_linear_workspace_bytes(pool.handle, n), dtype=torch.uint8, device=DEV)
+    x0 = case.x.to(DEV)
+
+    def chain():
+        x = x0
+        for i in range(L):
+            pool.linear(Ws[i], x, seg, variant=1, y=ys[i], ws=ws)
+            x = ys[i]
+
+    chain()
+    torch.cuda.synchronize()
+    eager = [y.clone() for y in ys]
+    ref_pool = O.pool_of_case(case)
+    for i in range(L):
+        xin = x0 if i == 0 else eager[i - 1]
+        y_ref = O.lora_linear(xin.cpu(), Ws[i].cpu(), ref_pool, case.idx.numpy())
+        assert_parity(eager[i].cpu(), y_ref, f"chained linear {i}")
+    words = seg_arrays(lib, seg)["nseg"]
+    assert words[2:].tolist() == [0, 0, 0, 0]
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            chain()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(L):
+            assert torch.equal(ys[i], eager[i]), f"graph replay of chained linear {i}"
+        assert seg_arrays(lib, seg)["nseg"][2:].tolist() == [0, 0, 0, 0]
+
+
 # ------------------------------------------------------------------------------------------
 # the five workloads
 # ------------------------------------------------------------------------------------------
