@@ -548,7 +548,7 @@ def segment_arrays(seg: lora_segments) -> dict:
         return ws[off:off + 4 * count].view(torch.int32)
 
     return {"perm": view(seg.perm_dev, n), "seg_start": view(seg.seg_start_dev, S + 2),
-            "seg_slot": view(seg.seg_slot_dev, S + 1), "nseg": view(seg.nseg_dev, 6),
+            "seg_slot": view(seg.seg_slot_dev, S + 1), "nseg": view(seg.nseg_dev, 4),
             "status": view(seg.status_dev, 1), "idx": view(seg.idx_dev, n), "items": view(seg.items_dev, 8 * n)}
 
 

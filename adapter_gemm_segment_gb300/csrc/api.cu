@@ -223,25 +223,19 @@ int linear_fwd_impl(lora_pool_t pool, const void* W_dev, const void* x_dev, void
 
     const bool tc = variant != kVariantCudaCore && tc_supported(pv, n);
     const bool fused = variant != LORA_VARIANT_SEPARATE;
-    // Fused decode batches compute the shrink inside the base GEMM's grid when that grid fits on
-    // the GPU at once: no shrink kernel, so each linear's GEMM follows the previous kernel
-    // directly (one dependency hop per linear instead of two).
-    const bool grid_shrink = tc && fused && n <= 256 && decode_grid_shrink_ok(pv, n);
-    // Otherwise a fused decode GEMM after the per-token shrink kernel follows it through the
-    // x-ready hand-off: the shrink releases it at once and publishes a value unique to this pair
-    // once every earlier kernel is complete, so the GEMM's weight stream and its B staging
-    // overlap the previous linear's tail.  Measured on GB300 (32 chained 4096 x 4096 fp16
-    // linears, us per linear with / without): r_max 8 at 16, 32, 64 tokens 13.44 / 14.09,
-    // 13.68 / 14.61, 13.58 / 15.17; r_max 64 at 16 tokens 16.49 / 16.67.  Behind the segmented
-    // shrink (r_max 64 at 64 tokens: many more CTAs, a longer shrink) it lost: 19.44 / 18.83.
-    const int xready =
-        (tc && fused && n <= 256 && !grid_shrink && !shrink_segmented(pv, n)) ? next_xready_value() : 0;
+    // A fused decode GEMM after the per-token shrink kernel follows it through the x-ready
+    // hand-off: the shrink releases it at once and publishes a value unique to this pair once
+    // every earlier kernel is complete, so the GEMM's weight stream and its B staging overlap
+    // the previous linear's tail.  Measured on GB300 (32 chained 4096 x 4096 fp16 linears, us
+    // per linear with / without): r_max 8 at 16, 32, 64 tokens 13.44 / 14.09, 13.68 / 14.61,
+    // 13.58 / 15.17; r_max 64 at 16 tokens 16.49 / 16.67.  Behind the segmented shrink (r_max 64
+    // at 64 tokens: many more CTAs, a longer shrink) it lost: 19.44 / 18.83.  At 1-8 tokens it
+    // also beat a shrink computed inside the GEMM's own grid (11.7-11.9 against 12.2-13.2).
+    const int xready = (tc && fused && n <= 256 && !shrink_segmented(pv, n)) ? next_xready_value() : 0;
     record_if(g_ev_before_shrink, st);
     int rc = LORA_OK;
     int s_parts = 1;
-    if (grid_shrink)
-        s_parts = shrink_parts(pv, n, false);
-    else if (tc && n > 256 && shrink_tc_supported(pv))
+    if (tc && n > 256 && shrink_tc_supported(pv))
         rc = launch_shrink_tc(pv, sv, x_dev, s_buf, st);
     else
         rc = launch_shrink(pv, sv, x_dev, s_buf, st, /*tiled=*/n > 256, &s_parts, xready);
@@ -249,7 +243,7 @@ int linear_fwd_impl(lora_pool_t pool, const void* W_dev, const void* x_dev, void
     record_if(g_ev_before_gemm, st);
     if (tc) {
         rc = launch_gemm_tc(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st, prefetch_dev, prefetch_bytes,
-                            nullptr, grid_shrink, xready);
+                            nullptr, xready);
     } else {
         rc = launch_gemm_simt(pv, sv, W_dev, x_dev, s_buf, s_parts, y_dev, fused, st);
     }

@@ -56,12 +56,11 @@ struct PoolView {
 };
 
 // Segments as the kernels see them (device pointers).
-// Words of the segment workspace's nseg array after the segment and item counts: the
-// in-grid shrink's hand-off counters {produced, consumed}, then the x-ready word a decode
-// shrink publishes for the GEMM after it and the count of that GEMM's CTAs that have read it.
-constexpr int kGridShrinkWords = 2;
-constexpr int kXreadyWord = 4;
-constexpr int kXreadyCount = 5;
+// Words of the segment workspace's nseg array after the segment and item counts: the x-ready
+// word a decode shrink publishes for the GEMM after it, and the count of that GEMM's CTAs that
+// have read it.
+constexpr int kXreadyWord = 2;
+constexpr int kXreadyCount = 3;
 
 struct SegView {
     const int32_t* perm;

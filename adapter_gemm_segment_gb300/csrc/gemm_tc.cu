@@ -67,13 +67,6 @@ struct DecodeArgs {
     const char* prefetch;  // optional range streamed into L2 once this CTA's accumulator is complete
     size_t prefetch_bytes;
     unsigned long long* stamp;  // benchmark instrumentation (nullptr: off)
-    // In-grid shrink: no shrink kernel precedes this grid.  After the grid-dependency wait the
-    // epilogue warps of every CTA compute the shrink's work units into s_out (== s_in) and hand
-    // it over through ctr = {produced, consumed} (in the segment workspace, zero on entry).
-    int grid_shrink;
-    const void* x;  // [n, h_in], read directly by the in-grid shrink
-    float* s_out;
-    int* ctr;
     // x-ready hand-off with the shrink kernel before this grid (nonzero: the value it publishes
     // in *xword once every earlier kernel is complete; xword[1] counts this grid's readers)
     int xready;
@@ -289,88 +282,6 @@ __device__ __forceinline__ void lora_batch8_pre(const uint4* __restrict__ Bp4, c
 //          CTA owns into that CTA's receive buffer (completion on the receiver's mbarrier); when
 //          the buffers do not fit, owners read the partials remotely instead.
 //  phase D: owners add the partials, the LoRA term and store y.  No global scratch.
-// In-grid shrink of the decode GEMM.  The work units of the segmented shrink -- (work item = up
-// to 4 sorted tokens of one adapter, 8-row group of r_max, K part) -- are dealt round robin over
-// the CTAs of the grid (CTA cta of n_ctas), and the 128 epilogue threads of a CTA compute one
-// unit together, as one CTA of the separate shrink kernel does: 8 features per thread and
-// sweep, so a part of up to 1024 features costs one round trip to memory.  A thread's 4 x 8
-// partial dot products (tokens x adapter rows) are reduced over its warp (reduce-scatter
-// butterfly: lane L ends with sum L = token L/8, row L%8), then over the 4 warps through red
-// [4][32], and scale * sum goes to s_out[(part * n + token) * r_max + row].  Row groups past the
-// adapter's true rank store zeros, as the separate shrink kernel does.
-template <typename T>
-__device__ __forceinline__ void grid_shrink_units(const DecodeArgs& a, int cta, int n_ctas, int et, float* red) {
-    const int lane = et & 31, w = et >> 5;
-    const int R = a.pool.R, h = a.pool.h_in, rg = R / 8, parts = a.s_parts, n = a.n;
-    const int n_items = __ldcg(a.seg.nseg + 1);
-    const int units = n_items * rg * parts;
-    const T* __restrict__ x = static_cast<const T*>(a.x);
-    const T* __restrict__ A = static_cast<const T*>(a.pool.A);
-    const int sweeps = ((h + 1023) / 1024 + parts - 1) / parts;  // the shrink kernels' K-part split
-    for (int u = cta; u < units; u += n_ctas) {
-        const int b = u / (rg * parts);
-        const int rem = u - b * rg * parts;
-        const int g = rem / parts, ks = rem - g * parts;
-        const int4 head = __ldcg(reinterpret_cast<const int4*>(a.seg.items + (size_t)b * 8));  // slot, count, tok0, tok1
-        const int4 tail = __ldcg(reinterpret_cast<const int4*>(a.seg.items + (size_t)b * 8 + 4));  // tok2, tok3, rank
-        const int slot = head.x, nt = head.y;
-        const int tok[4] = {head.z, head.w, tail.x, tail.y};
-        if (g * 8 >= tail.z && g * 8 >= a.pool.table[slot].rank) {  // rows past the true rank: A is zero
-            if (et < nt * 8) {
-                const int q = et >> 3;
-                const int t = q == 0 ? head.z : q == 1 ? head.w : q == 2 ? tail.x : tail.y;
-                a.s_out[((size_t)ks * n + t) * R + g * 8 + (et & 7)] = 0.f;
-            }
-            continue;  // uniform over the CTA: the condition depends on the unit only
-        }
-        const int k_beg = ks * sweeps * 1024;
-        const int k_end = min(h, k_beg + sweeps * 1024);
-        const T* Ab = A + ((size_t)slot * R + (size_t)g * 8) * h;
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = 0.f;
-        for (int k = k_beg + et * 8; k < k_end; k += 1024) {
-            uint4 av[8], xv[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) xv[q] = __ldcg(reinterpret_cast<const uint4*>(x + (size_t)tok[q] * h + k));
-#pragma unroll
-            for (int r = 0; r < 8; ++r) av[r] = __ldg(reinterpret_cast<const uint4*>(Ab + (size_t)r * h + k));
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float xf[8];
-                unpack8<T>(xv[q], xf);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    float af[8];
-                    unpack8<T>(av[r], af);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[q * 8 + r] = fmaf(xf[e], af[e], v[q * 8 + r]);
-                }
-            }
-        }
-#pragma unroll
-        for (int step = 0; step < 5; ++step) {
-            const int half = 16 >> step, off = 16 >> step;
-            const bool up = (lane & off) != 0;
-#pragma unroll
-            for (int e = 0; e < half; ++e) {
-                const float send = up ? v[e] : v[e + half];
-                const float keepv = up ? v[e + half] : v[e];
-                v[e] = keepv + __shfl_xor_sync(0xffffffffu, send, off);
-            }
-        }
-        red[w * 32 + lane] = v[0];
-        named_bar_sync(1, 128);
-        if (et < nt * 8) {
-            const int q = et >> 3;
-            const int t = q == 0 ? head.z : q == 1 ? head.w : q == 2 ? tail.x : tail.y;
-            const float sum = red[et] + red[32 + et] + red[64 + et] + red[96 + et];
-            a.s_out[((size_t)ks * n + t) * R + g * 8 + (et & 7)] = a.pool.table[slot].scale * sum;
-        }
-        named_bar_sync(1, 128);  // red is reused by the next unit
-    }
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -393,8 +304,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int* dlist = dloc_sm + per;                                                 // [per]
     int* fidx_sm = dlist + per;                                                 // [per]
     int* pre_sm = fidx_sm + per;  // [1 + 2 kMaxPre]: staged slots; their uint4 offsets; chunks per row
-    float* red_sm = reinterpret_cast<float*>(pre_sm + 1 + 2 * kMaxPre);  // [4][32]: in-grid shrink reduction
-    float* S_sm = smem_align(red_sm + 128, 16);  // [s_parts][per][R]
+    float* S_sm = smem_align(reinterpret_cast<float*>(pre_sm + 1 + 2 * kMaxPre), 16);  // [s_parts][per][R]
     float* L_sm = S_sm + (size_t)a.s_parts * per * R;                            // [per][128] if use_lsm
     T* Bpre = smem_align(reinterpret_cast<T*>(L_sm + (use_lsm ? (size_t)per * BM : 0)), 128);  // bpre_bytes
     uint64_t* full = smem_align(reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(Bpre) + a.bpre_bytes), 8);
@@ -448,9 +358,9 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     };
     // The producer thread initialises the barriers and fills the ring right away, so the first
     // HBM round trip overlaps the TMEM allocation and the CTA-wide barrier below.  With the
-    // in-grid shrink or the x-ready hand-off, the previous linear may still be running, so only
-    // the W boxes go out now (a weight is never written by the kernels of the linear chain);
-    // the x boxes follow the grid-dependency wait or the hand-off.
+    // x-ready hand-off the previous linear may still be running, so only the W boxes go out now
+    // (a weight is never written by the kernels of the linear chain); the x boxes follow the
+    // hand-off.
     const int pre = min(stages, nkb);
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -466,7 +376,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmX);
         for (int i = 0; i < pre; ++i) {
-            if (a.grid_shrink || a.xready)
+            if (a.xready)
                 issue_w(i);
             else
                 issue_stage(i);
@@ -495,14 +405,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // Without a hand-off, W and x are complete when this grid starts if a shrink kernel
         // precedes it in the stream: it releases its dependents only after its own
         // grid-dependency wait, and only the shrink output (read by the epilogue warps) needs
-        // this grid's wait.  With the in-grid shrink this grid follows the previous kernel
-        // directly and waits itself before the first x box; with the x-ready hand-off it reads
-        // x once the shrink has published the pair's value.
+        // this grid's wait.  With the x-ready hand-off the shrink released this grid at its
+        // start, and x is read once the shrink has published the pair's value.
         if (lane == 0) {
-            if (a.grid_shrink) {
-                pdl_wait();
-                for (int i = 0; i < pre; ++i) issue_x(i);
-            } else if (a.xready) {
+            if (a.xready) {
                 // The shrink kernel before this grid released it at its start and publishes the
                 // value once every earlier kernel is complete: x may then be read (through TMA,
                 // after a proxy fence); the weight boxes are already on their way.  The last CTA
@@ -573,8 +479,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
     } else {
         // ---- phase A (overlaps the main loop): stage this CTA's LoRA operands ----
-        // s (or x for the in-grid shrink), idx and the status word come from earlier kernels.
-        // With the x-ready hand-off every kernel before the shrink is complete once the producer
+        // s, idx and the status word come from earlier kernels.  With the x-ready hand-off every kernel before the shrink is complete once the producer
         // has seen its signal: the segments are read then, and only s waits for this grid's
         // dependency wait (below, after the B tiles are on their way).
         if (a.xready) {
@@ -584,48 +489,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         if (et == 0) flags[3] = flags[0] ? LORA_ETIMEOUT : __ldcg(a.seg.status);
         named_bar_sync(1, 128);
-        const int n_ctas = gridDim.x * gridDim.y;
-        // In-grid shrink: every CTA computes its share of the shrink units, then counts itself
-        // produced -- also with nothing to do or an error status, so that the hand-off always
-        // completes.  The output is complete once every CTA has counted itself produced
-        // (bounded wait: on timeout the status word says so and y is not written).  Then the
-        // CTA counts itself consumed; the last one resets both counters for the next linear.
-        auto wait_produced = [&]() {
-            if (et == 0) {
-                const unsigned long long t0w = globaltimer();
-                int got = 0;
-                while ((got = ld_acquire_gpu(&a.ctr[0])) < n_ctas) {
-                    if (globaltimer() - t0w > kWaitLimitNs) break;
-                    __nanosleep(64);
-                }
-                if (got < n_ctas) {
-                    flags[0] = 1;
-                    report_timeout_status(a.seg.status);
-                }
-            }
-            named_bar_sync(1, 128);
-        };
-        auto consume = [&]() {
-            if (et == 0 && atomicAdd(&a.ctr[1], 1) == n_ctas - 1) {
-                atomicExch(&a.ctr[0], 0);
-                atomicExch(&a.ctr[1], 0);
-            }
-        };
-        auto produce = [&](bool work) {
-            if (work) grid_shrink_units<T>(a, blockIdx.y * gridDim.x + blockIdx.x, n_ctas, et, red_sm);
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (et == 0) atomicAdd(&a.ctr[0], 1);
-        };
         const bool lora = flags[3] == LORA_OK && a.fuse;
         // With the x-ready hand-off, this grid completes only after the shrink before it (as
         // every later kernel's dependency wait assumes): the LoRA path waits below, this one here.
         if (!lora && a.xready) pdl_wait();
-        if (!lora && a.grid_shrink) {
-            produce(false);
-            wait_produced();
-            consume();
-        }
         if (lora) {
             for (int q = et; q < cnt; q += 128) slot_sm[q] = __ldcg(a.seg.idx + t0 + q);
             named_bar_sync(1, 128);
@@ -686,11 +553,10 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         ++ns;
                     }
                     pre_sm[0] = ns;
-                    // bulk copies of the owned tokens' shrink parts (unless the in-grid shrink
-                    // is still writing them, or they come after this grid's dependency wait),
-                    // then one TMA box per staged slot and 8-column chunk: [128 feature rows][8
-                    // columns] of B
-                    const uint32_t sb = (cnt > 0 && !a.grid_shrink && !a.xready) ? a.s_parts * s_bytes : 0;
+                    // bulk copies of the owned tokens' shrink parts (unless they come after this
+                    // grid's dependency wait), then one TMA box per staged slot and 8-column
+                    // chunk: [128 feature rows][8 columns] of B
+                    const uint32_t sb = (cnt > 0 && !a.xready) ? a.s_parts * s_bytes : 0;
                     if (a.xready)
                         mbar_expect_tx(lbar, static_cast<uint32_t>(off) * 16);  // s: arrival below
                     else
@@ -708,7 +574,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint32_t b_bytes = static_cast<uint32_t>(rows_valid * R * 2);
                     const int ns = min(min(running, kMaxPre), a.bpre_bytes / (BM * R * 2));
                     pre_sm[0] = ns;
-                    const uint32_t sb = (cnt > 0 && !a.grid_shrink && !a.xready) ? a.s_parts * s_bytes : 0;
+                    const uint32_t sb = (cnt > 0 && !a.xready) ? a.s_parts * s_bytes : 0;
                     if (a.xready)
                         mbar_expect_tx(lbar, ns * b_bytes);  // s: arrival below
                     else
@@ -731,16 +597,6 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         for (int k = 0; k < a.s_parts; ++k)
                             bulk_g2s(S_sm + (size_t)k * per * R, a.s_in + ((size_t)k * n + t0) * R, s_bytes, lbar);
                 }
-            }
-            if (a.grid_shrink) {  // this CTA's shrink share; the owned tokens' parts once the grid is done
-                produce(true);
-                wait_produced();
-                for (int e = et; e < a.s_parts * cnt * R; e += 128) {
-                    const int k = e / (cnt * R), r = e - k * cnt * R;
-                    S_sm[(size_t)k * per * R + r] = __ldcg(a.s_in + ((size_t)k * n + t0) * R + r);
-                }
-                named_bar_sync(1, 128);
-                consume();
             }
             const int Dg = pre_sm[0];
             const bool staged = mbar_wait(lbar, 0, flags);
@@ -1467,7 +1323,7 @@ static DecodePlan plan_decode(const PoolView& pv, int n, int s_parts) {
     const bool use_lsm = per <= kLsmMaxTokens;
     // dedicated region: 4 int arrays, the staged-slot table, s parts [s_parts][per][R], LoRA
     // term [per][128] (small shares), alignment, barriers
-    const size_t fixed = (size_t)per * 4 * 4 + (1 + 2 * kMaxPre) * 4 + 128 * 4 + 16 + (size_t)s_parts * per * pv.R * 4 +
+    const size_t fixed = (size_t)per * 4 * 4 + (1 + 2 * kMaxPre) * 4 + 16 + (size_t)s_parts * per * pv.R * 4 +
                          (use_lsm ? (size_t)per * BM * 4 : 0) + 128 + 2 * 1024;
     const size_t slot_b = (size_t)BM * pv.R * 2;  // one B tile at r_max (the late path's unit)
     // B tiles staged during the main loop are kept at their slots' true ranks: k slots need at
@@ -1539,62 +1395,10 @@ int decode_fused_fits(const PoolView& pv, int n) {
     return per <= tc::kLsmMaxTokens && (p.dpre >= std::min(per, pv.S) || pv.R <= 16) ? 1 : 0;
 }
 
-// Clusters of the decode kernel (one CTA per SM at its shared-memory size) that the GPU holds
-// at once, for a cluster of `splits` CTAs (queried once per shape).
-static int decode_max_clusters(const tc::DecodePlan& p) {
-    static std::mutex mu;
-    static std::vector<std::pair<std::pair<size_t, int>, int>> cache;
-    std::lock_guard<std::mutex> lock(mu);
-    for (const auto& c : cache)
-        if (c.first.first == p.smem && c.first.second == p.splits) return c.second;
-    int clusters = 0;
-    if (cudaFuncSetAttribute(tc::gemm_decode_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) ==
-        cudaSuccess) {
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof(cfg));
-        cfg.gridDim = dim3(p.m_tiles, p.splits);
-        cfg.blockDim = dim3(tc::kThreads);
-        cfg.dynamicSmemBytes = p.smem;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = p.splits;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)tc::gemm_decode_kernel<__half>, &cfg) != cudaSuccess)
-            clusters = 0;
-    }
-    (void)cudaGetLastError();  // a refused query only disables the in-grid shrink
-    cache.push_back({{p.smem, p.splits}, clusters});
-    return clusters;
-}
-
-// Measured on GB300 (32 chained 4096 x 4096 fp16 linears, 100 rank-8 adapters, one box, us per
-// linear with the in-grid shrink / with the shrink kernel): 1 token 12.04 / 13.43, 2: 12.35 /
-// 13.49, 4: 12.60 / 13.62, 8: 12.83 / 13.62, 16: 14.22 / 14.01, 32: 14.83 / 14.46, 64: 15.63 /
-// 14.90.  From 16 tokens on, the hand-off of the shrink output between the grid's CTAs costs
-// more than the shrink kernel's extra dependency hop.
-constexpr int kGridShrinkMaxTokens = 8;
-
-int decode_grid_shrink_ok(const PoolView& pv, int n) {
-    if (n <= 0 || n > kGridShrinkMaxTokens || !tc_supported(pv, n)) return 0;
-    const int parts = shrink_parts(pv, n, false);
-    const tc::DecodePlan p = tc::plan_decode(pv, n, parts);
-    // Its work units (at most one shrink item per LoRA token and, per segment, one partial item
-    // beyond n / 4) must come to at most 3 per CTA: each costs the CTA's epilogue threads a round
-    // trip to memory, and more would keep the shrink running past the main loop.
-    const long long items = std::min(n, pv.S) + (n + 3) / 4;
-    const long long units = items * (pv.R / 8) * parts;
-    if (units > 3LL * p.m_tiles * p.splits) return 0;
-    // every CTA waits for the shrink shares of all the others: the whole grid must be resident
-    return p.m_tiles <= decode_max_clusters(p) ? 1 : 0;
-}
-
 template <typename T>
 static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in,
                        int s_parts, void* y, bool fuse, const void* prefetch, size_t prefetch_bytes,
-                       const GroupView* grp, cudaStream_t st, bool grid_shrink, int xready) {
+                       const GroupView* grp, cudaStream_t st, int xready) {
     using namespace tc;
     const int n = sv.n;
     if (n == 0) return LORA_OK;
@@ -1649,12 +1453,11 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
         a.prefetch = static_cast<const char*>(prefetch);
         a.prefetch_bytes = prefetch ? prefetch_bytes : 0;
         a.stamp = take_kernel_stamp();
-        a.grid_shrink = grid_shrink && fuse && g1.count == 1 ? 1 : 0;
-        a.xready = a.grid_shrink ? 0 : xready;
+        // the shrink before a hand-off does not wait for x itself: only this fused single-slice
+        // GEMM reads x after its published value
+        if (xready && !(fuse && g1.count == 1)) return set_error(LORA_EINVAL, "internal: x-ready hand-off");
+        a.xready = xready;
         a.xword = const_cast<int*>(sv.nseg) + kXreadyWord;
-        a.x = x;
-        a.s_out = const_cast<float*>(s_in);
-        a.ctr = const_cast<int*>(sv.nseg) + 2;
         static bool attr_set = false;
         if (!attr_set) {
             LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1775,12 +1578,12 @@ int launch_gemm_tall(const PoolView& pv, const SegView& sv, const void* W, const
 
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
                    void* y, bool fuse, cudaStream_t st, const void* prefetch, size_t prefetch_bytes,
-                   const GroupView* grp, bool grid_shrink, int xready) {
+                   const GroupView* grp, int xready) {
     if (pv.dtype == LORA_F16)
         return launch_tc_t<__half>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st,
-                                   grid_shrink, xready);
+                                   xready);
     return launch_tc_t<__nv_bfloat16>(pv, sv, W, x, s_in, s_parts, y, fuse, prefetch, prefetch_bytes, grp, st,
-                                      grid_shrink, xready);
+                                      xready);
 }
 
 }  // namespace lora

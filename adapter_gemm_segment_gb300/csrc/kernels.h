@@ -55,17 +55,12 @@ int tc_supported(const PoolView& pv, int n);
 // has published the value.
 int launch_gemm_tc(const PoolView& pv, const SegView& sv, const void* W, const void* x, const float* s_in, int s_parts,
                    void* y, bool fuse, cudaStream_t st, const void* prefetch = nullptr, size_t prefetch_bytes = 0,
-                   const GroupView* grp = nullptr, bool grid_shrink = false, int xready = 0);
+                   const GroupView* grp = nullptr, int xready = 0);
 
 // The launch sequence of one LoRA-augmented linear (lora_linear_fwd and its variants), after the
 // caller's arguments were checked; s_buf receives the shrink output.
 int linear_fwd_impl(lora_pool_t pool, const void* W_dev, const void* x_dev, void* y_dev, const lora_segments* seg,
                     int variant, float* s_buf, const void* prefetch_dev, size_t prefetch_bytes, cudaStream_t st);
-
-// Whether the fused decode GEMM for n tokens on this pool can compute the shrink inside its own
-// grid (no shrink kernel): its whole grid fits on the GPU at once, which the hand-off of the
-// shrink output between its CTAs needs.  s_in of launch_gemm_tc is then written, not read.
-int decode_grid_shrink_ok(const PoolView& pv, int n);
 
 // Base GEMM y = x W^T (no LoRA term) with 256 W rows per CTA, two M=128 MMAs sharing each x
 // tile, full K per CTA (batches of up to 256 tokens); y has row stride ldy.

@@ -180,12 +180,9 @@ segment_kernel(const int32_t* __restrict__ idx, int n, const SlotEntry* __restri
     constexpr int U = 4;  // tokens per thread whose loads are issued together
 
     pdl_wait();  // idx and the slot table may come from earlier kernels in the stream
-    // hand-off words of the decode GEMMs (the in-grid shrink's produced / consumed counters, the
-    // x-ready word and its read count); each GEMM leaves its words at zero for the next linear
-    // over these segments
+    // hand-off words of the decode kernels (the x-ready word and its read count); each fused
+    // decode GEMM leaves them at zero for the next linear over these segments
     if (tid == 0) {
-        nseg_out[2] = 0;
-        nseg_out[3] = 0;
         nseg_out[kXreadyWord] = 0;
         nseg_out[kXreadyCount] = 0;
     }

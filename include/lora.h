@@ -94,8 +94,8 @@ typedef struct lora_pool* lora_pool_t;
  *   perm_dev[j]       original position of the j-th token in sorted order     [n]
  *   seg_start_dev[i]  first sorted position of segment i; seg_start[nseg] = n  [n_slots+2]
  *   seg_slot_dev[i]   slot of segment i (-1 for the base-only run)            [n_slots+1]
- *   nseg_dev          number of segments, the number of shrink items, then four
- *                     words the decode kernels use internally                [6]
+ *   nseg_dev          number of segments, the number of shrink items, then two
+ *                     words the decode kernels use internally                [4]
  *   status_dev        LORA_OK or LORA_EIDX                                    [1]
  *   idx_dev           copy of the batch's idx (original order)               [n]
  *   items_dev         shrink work items: every adapter segment cut into runs of up to 4
@@ -104,9 +104,8 @@ typedef struct lora_pool* lora_pool_t;
  *                     hint -- kernels of another pool check their own slot table) 
  * Segments are rebuilt once per batch and reused by every linear layer that runs
  * over that batch, as long as the workspace stays alive and unmodified.  The linears that
- * use one segment table run on one stream, one after another: decode GEMMs that compute
- * the shrink inside their own grid hand it over through two of the words above, and a decode
- * shrink kernel tells the fused GEMM after it through the other two when x may be read. */
+ * use one segment table run on one stream, one after another (a decode shrink kernel tells
+ * the fused GEMM after it through the two words above when x may be read). */
 typedef struct {
     int32_t* perm_dev;
     int32_t* seg_start_dev;
