@@ -867,7 +867,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint64_t* acc_empty = acc_full + 2;   // [2]
     uint64_t* lora_free = acc_empty + 2;  // the LoRA block's stage is free (one phase per tile)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lora_free + 1);
-    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [16]
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [20]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = a.m_tiles * a.n_tiles;
@@ -1002,6 +1002,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         const int et = threadIdx.x - 64;  // 0..127
         volatile int* red = flags + 2;   // [4]: per-warp minima
         volatile int* dsl = flags + 8;   // [8]: the tile's distinct adapters
+        volatile int* redx = flags + 16;  // [4]: per-warp maxima
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
             const int buf = local & 1;
             if (!waited) {
@@ -1019,12 +1020,18 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 const int qa = group_slice_of_col(a.grp, n0);
                 const int qb = group_slice_of_col(a.grp, min(n0 + BN, ldy) - 1);
                 const int dmax = 64 / R;
-                // distinct adapters of the tile in increasing order (uniform over the 128 threads)
+                // distinct adapters of the tile in increasing order (uniform over the 128 threads);
+                // the first round also takes the maximum, so that a tile of one adapter (the
+                // common prefill case) needs no second round
                 int mine = -1, D = 0;
                 for (int d = 0; d <= dmax; ++d) {
                     const int cand = __reduce_min_sync(0xffffffffu, (slot_r >= 0 && mine < 0) ? slot_r : INT_MAX);
+                    const int candx = d == 0 ? __reduce_max_sync(0xffffffffu, slot_r) : -1;
                     named_bar_sync(1, 128);  // the previous round has read red
-                    if (lane == 0) red[q] = cand;
+                    if (lane == 0) {
+                        red[q] = cand;
+                        redx[q] = candx;
+                    }
                     named_bar_sync(1, 128);
                     const int m = min(min(red[0], red[1]), min(red[2], red[3]));
                     if (m == INT_MAX) break;
@@ -1032,6 +1039,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     if (d == dmax) break;  // more adapters than the block holds
                     if (slot_r == m) mine = d;
                     if (et == 0) dsl[d] = m;
+                    if (d == 0 && m == max(max(redx[0], redx[1]), max(redx[2], redx[3]))) break;  // one adapter
                 }
                 const int lk = (D == 0 || D > dmax || qa != qb) ? 0 : (D * R + 15) / 16 * 16;
                 lora_done = lk > 0;
@@ -1513,8 +1521,8 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     if (rc) return rc;
     rc = make_map(&mW, W, bf16, pv.h_in, pv.h_out, kPrefillBN);
     if (rc) return rc;
-    // barriers (2 per stage, 4 accumulator, lora_free), the TMEM address and 16 flag words
-    if ((2 * a.stages + 5) * 8 + 4 + 16 * 4 > 256) return set_error(LORA_EINVAL, "internal: prefill barrier area");
+    // barriers (2 per stage, 4 accumulator, lora_free), the TMEM address and 20 flag words
+    if ((2 * a.stages + 5) * 8 + 4 + 20 * 4 > 256) return set_error(LORA_EINVAL, "internal: prefill barrier area");
     const size_t smem = (size_t)a.stages * stage_bytes + 1024 + 256;
     static bool attr = false;
     if (!attr) {
