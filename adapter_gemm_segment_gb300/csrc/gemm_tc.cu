@@ -852,7 +852,7 @@ gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                    const PrefillArgs a) {
+                    const __grid_constant__ CUtensorMap tmY, const PrefillArgs a) {
     constexpr int BN = kPrefillBN;
     stamp_start(a.stamp);
     extern __shared__ uint8_t smem_raw[];
@@ -868,6 +868,8 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint64_t* lora_free = acc_empty + 2;  // the LoRA block's stage is free (one phase per tile)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lora_free + 1);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [20]
+    // y staging of the epilogue: [4 warps][2 buffers][32 rows][32 columns] 16-bit, after the barriers
+    T* ystage = reinterpret_cast<T*>(smem + stages * stage_bytes + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = a.m_tiles * a.n_tiles;
@@ -999,6 +1001,7 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         bool waited = false;
         int status = LORA_OK;
         int local = 0;
+        int ybuf = 0;  // this warp's staging buffer for the next 32 columns
         const int et = threadIdx.x - 64;  // 0..127
         volatile int* red = flags + 2;   // [4]: per-warp minima
         volatile int* dsl = flags + 8;   // [8]: the tile's distinct adapters
@@ -1099,21 +1102,25 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             const int t = m0 + q * 32 + lane;
             const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
             const int slot = (a.fuse && !lora_done && t < n) ? __ldcg(a.seg.idx + t) : -1;
-            // 32 columns per round: both TMEM loads, one wait, then two 16-column pieces
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            // 32 columns per round: both TMEM loads, one wait, the two 16-column pieces into
+            // this warp's staging buffer (its 32 token rows), then one TMA store of the buffer
+            // (rows and columns outside y are clipped; nothing is stored with an error status)
+            for (int c0 = 0; c0 < BN; c0 += 32, ybuf ^= 1) {
                 uint32_t r[32];
                 __syncwarp();
                 tmem_ld16(taddr + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
                 tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
                 tmem_ld_wait();
+                T* Ys = ystage + (size_t)(q * 2 + ybuf) * 32 * 32;
+                if (lane == 0) bulk_wait_group_read1();  // this buffer's previous store has read it
+                __syncwarp();
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int col = n0 + c0 + 16 * hf;  // column of y
-                    if (status != LORA_OK || t >= n || col >= ldy) continue;  // after the warp-wide loads
                     float v[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[16 * hf + c]);
-                    if (slot >= 0) {
+                    if (slot >= 0 && col < ldy) {
                         // the slice owning these 16 columns (slice boundaries are multiples of 16)
                         const SliceRef sl = group_slice(a.grp, group_slice_of_col(a.grp, col));
                         const float* srow = a.s_in + sl.s_off + (size_t)t * R;
@@ -1144,17 +1151,23 @@ gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                             }
                         }
                     }
-                    uint4* yp = reinterpret_cast<uint4*>(y + (size_t)t * ldy + col);
-                    yp[0] = make_uint4(pack2<T>(v[0], v[1]), pack2<T>(v[2], v[3]), pack2<T>(v[4], v[5]),
+                    uint4* yr = reinterpret_cast<uint4*>(Ys + (size_t)lane * 32 + 16 * hf);
+                    yr[0] = make_uint4(pack2<T>(v[0], v[1]), pack2<T>(v[2], v[3]), pack2<T>(v[4], v[5]),
                                        pack2<T>(v[6], v[7]));
-                    if (col + 16 <= ldy)  // else h_out (a multiple of 8) leaves one half-chunk
-                        yp[1] = make_uint4(pack2<T>(v[8], v[9]), pack2<T>(v[10], v[11]), pack2<T>(v[12], v[13]),
-                                           pack2<T>(v[14], v[15]));
+                    yr[1] = make_uint4(pack2<T>(v[8], v[9]), pack2<T>(v[10], v[11]), pack2<T>(v[12], v[13]),
+                                       pack2<T>(v[14], v[15]));
+                }
+                fence_proxy_async_smem();  // read by the TMA store
+                __syncwarp();
+                if (lane == 0 && status == LORA_OK && n0 + c0 < ldy && m0 + q * 32 < n) {
+                    tma_store_2d(&tmY, Ys, n0 + c0, m0 + q * 32);
+                    bulk_commit_group();
                 }
             }
             tc_fence_before();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
+        if (lane == 0) bulk_wait_group_read0();  // the staging buffers stay until their stores have read them
     }
     tc_fence_before();
     __syncthreads();
@@ -1523,16 +1536,19 @@ static int launch_tc_t(const PoolView& pv, const SegView& sv, const void* W, con
     if (rc) return rc;
     // barriers (2 per stage, 4 accumulator, lora_free), the TMEM address and 20 flag words
     if ((2 * a.stages + 5) * 8 + 4 + 20 * 4 > 256) return set_error(LORA_EINVAL, "internal: prefill barrier area");
-    const size_t smem = (size_t)a.stages * stage_bytes + 1024 + 256;
+    const size_t smem = (size_t)a.stages * stage_bytes + 1024 + 256 + 4 * 2 * 32 * 32 * 2;  // + y staging
+    CUtensorMap mY;
+    rc = make_map_plain(&mY, y, bf16, g1.ldy, n, 32, 32, g1.ldy);
+    if (rc) return rc;
     static bool attr = false;
     if (!attr) {
         LORA_CUDA_TRY(cudaFuncSetAttribute(gemm_prefill_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemBudget + 8 * 1024));
+                                           227 * 1024));
         attr = true;
     }
     const int total = a.m_tiles * a.n_tiles;
     const int grid = std::min(total, num_sms());
-    void* args[] = {(void*)&mX, (void*)&mW, (void*)&a};
+    void* args[] = {(void*)&mX, (void*)&mW, (void*)&mY, (void*)&a};
     LORA_CUDA_TRY(launch_pdl((const void*)gemm_prefill_kernel<T>, dim3(grid), dim3(kThreads), smem, st, args));
     return LORA_OK;
 }
