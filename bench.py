@@ -32,7 +32,7 @@ launch in the chained graph; the serialised CUDA-event figure beside it), end-to
 with pinned host buffers and host<->device copies inside the timed region, the CPU oracle
 timed on the host cores (cpu_baseline), SM clocks sampled during the timed region, and the
 tensor-concatenation figures of the batch (concat_metrics).
-`--impl reference` times the CPU oracle alone (the reference arm of this build).
+`--impl reference` times the CPU oracle alone (the benchmark's reference arm: the pages hold no code to run).
 """
 from __future__ import annotations
 

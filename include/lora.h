@@ -67,7 +67,7 @@ typedef enum {
     LORA_ENOSPACE = -5, /* caller buffer or workspace too small */
     LORA_EIDX = -6,     /* (device) idx outside [-1, n_slots) or naming an empty slot */
     LORA_ECUDA = -7,    /* a CUDA runtime call failed */
-    LORA_EUNSUP = -8,   /* shape/dtype combination this build does not support */
+    LORA_EUNSUP = -8,   /* shape/dtype combination the library does not support */
     LORA_ETIMEOUT = -9  /* (device) a pipeline wait exceeded its time limit; output invalid */
 } lora_status;
 
