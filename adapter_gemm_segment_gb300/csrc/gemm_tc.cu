@@ -17,11 +17,14 @@
 // to fill the GPU: each CTA parks its float32 partial tile in shared memory, the partials are
 // exchanged by shared-to-remote-shared bulk copies (DSMEM) so that each CTA of the cluster owns
 // a slice of the tokens, and each CTA sums its slice in split order, adds the LoRA term and
-// stores its tokens of y with a TMA store.
+// stores its tokens of y with a TMA store.  Behind the per-token shrink kernel the GEMM is
+// released at the shrink's start and reads x once the shrink has published the pair's x-ready
+// value (its weight stream overlaps the previous linear's tail).
 //
 // Prefill (n > 256): 128-token x 256-feature tiles, persistent CTAs over the tile list,
 // double-buffered accumulators (2 x 256 TMEM columns) so the epilogue of one tile overlaps the
-// main loop of the next.
+// main loop of the next.  A tile's LoRA term is one more tensor-core K block when its adapters
+// fit one (below), and y leaves through shared memory and TMA stores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
