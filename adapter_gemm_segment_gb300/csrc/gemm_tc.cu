@@ -1408,10 +1408,10 @@ int tc_supported(const PoolView& pv, int n) {
 // either the B rows of every adapter those tokens can use are staged during the main loop
 // (pre-staged slots >= min(owned tokens, n_slots)) or r_max is at most 16, where the epilogue's
 // late SIMT groups load little.  Measured on GB300 (32 chained 4096 x 4096 fp16 linears, us per
-// linear fused / separate): r_max 8 at 64, 96, 128 tokens 15.0 / 19.2, 19.0 / 24.6, 22.7 / 25.8
-// and at 192, 256 tokens (48 and 64 owned tokens) 39.3 / 31.9, 38.5 / 32.4; r_max 64 on 6
-// adapters at 64, 96 tokens 18.5 / 24.8, 22.1 / 30.3 and at 128, 256 tokens (B tiles of 6
-// slots at r_max 64 do not all fit beside the pipeline) 52.6 / 38.1, 84.4 / 44.7.
+// linear fused / separate): r_max 8 at 64, 96, 128 tokens 13.1 / 19.4, 16.7 / 24.6, 22.2 / 25.9
+// and at 192, 256 tokens (48 and 64 owned tokens) 31.0 / 31.9, 38.4 / 32.4; r_max 64 on 6
+// adapters at 64, 96 tokens 18.2 / 24.9, 21.7 / 30.2 and at 128, 256 tokens (B tiles of 6
+// slots at r_max 64 do not all fit beside the pipeline) 52.3 / 37.9, 84.9 / 44.7.
 int decode_fused_fits(const PoolView& pv, int n) {
     if (n <= 0 || n > tc::kDecodeMaxN || !tc_supported(pv, n)) return 0;
     const tc::DecodePlan p = tc::plan_decode(pv, n, shrink_parts(pv, n, false));
